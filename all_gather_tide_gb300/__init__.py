@@ -1,0 +1,265 @@
+"""GB300 (sm_103a) layout-aware reduce-scatter and all-gather placement for FSDP2 groups.
+
+A thin ctypes binding of ``libtide.so`` (C ABI in ``include/tide.h``).  Functions carry the C
+names; they only marshal arguments (tensors -> device pointers, stream objects -> handles) and
+turn negative statuses into :class:`TideError`.  Every step of the path runs in the library's
+CUDA kernels or copy-engine calls; there is no Python or CPU fallback, and importing a function
+fails loudly if the library has not been built.
+
+"TIDE" is "The Endgame of FSDP Communication: Layout-Aware Collectives on Copy Engines, RDMA, and
+NVSwitch" (arXiv 2610.38228): the reduce-scatter is its TIDE-RS (abstract; Fig. 2b), the
+placement its TIDE-AG landing (abstract; Fig. 5b), the layout its Table 2.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtide.so")
+
+TIDE_OK = 0
+TIDE_EINVAL = -1
+TIDE_EALIGN = -2
+TIDE_ELAYOUT = -3
+TIDE_ECUDA = -4
+TIDE_ENOMEM = -5
+TIDE_ERANGE = -6
+TIDE_FLAG_VEC_STRICT = 0x1
+TIDE_FLAG_CE_STRICT = 0x2
+
+_lib = None
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_vp = ctypes.c_void_p
+_vpp = ctypes.POINTER(ctypes.c_void_p)
+
+# name -> (restype, argtypes); every symbol declared in include/tide.h
+SIGNATURES = {
+    "tide_plan_layout": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _i64p, _i64p, _i64p, _i64p, _i64p]),
+    "tide_group_create": (ctypes.c_int, [_vpp, ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, ctypes.c_uint32]),
+    "tide_group_destroy": (ctypes.c_int, [_vp]),
+    "tide_group_shard_elems": (ctypes.c_int, [_vp, _i64p]),
+    "tide_group_unsharded_elems": (ctypes.c_int, [_vp, _i64p]),
+    "tide_group_param_layout": (ctypes.c_int, [_vp, ctypes.c_int32, _i64p, _i64p]),
+    "tide_group_valid_rows": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32, _i64p]),
+    "tide_group_set_ctas": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32]),
+    "tide_group_get_ctas": (ctypes.c_int, [_vp, _i32p, _i32p]),
+    "tide_reduce_scatter": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
+    "tide_all_gather": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
+    "tide_all_gather_ce": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
+    "tide_group_last_ce_copies": (ctypes.c_int, [_vp, _i64p, _i32p]),
+    "tide_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "tide_last_cuda_error": (ctypes.c_int, []),
+    "tide_version": (ctypes.c_int, []),
+}
+
+
+class TideError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = lib().tide_strerror(status).decode()
+        if status == TIDE_ECUDA:
+            msg += f" (cudaError {lib().tide_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [{status}]")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with `python -m all_gather_tide_gb300.build` "
+                               "(or __graft_entry__.build()); there is no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != TIDE_OK:
+        raise TideError(status, where)
+
+
+def _ptr(x) -> int:
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _ptr_array(xs: Sequence) -> ctypes.Array:
+    return (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _i64_array(xs: Sequence[int]):
+    return (ctypes.c_int64 * len(xs))(*[int(x) for x in xs])
+
+
+# ---- C-named functions ------------------------------------------------------------------------
+
+
+def tide_version() -> int:
+    return lib().tide_version()
+
+
+def tide_strerror(status: int) -> str:
+    return lib().tide_strerror(status).decode()
+
+
+def tide_last_cuda_error() -> int:
+    return lib().tide_last_cuda_error()
+
+
+def tide_plan_layout(R: int, rows: Sequence[int], row_len: Sequence[int]):
+    """Host-only planner: returns (m, s, o, S, U) as Python lists / ints."""
+    P = len(rows)
+    m, s, o = (ctypes.c_int64 * P)(), (ctypes.c_int64 * P)(), (ctypes.c_int64 * P)()
+    S, U = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().tide_plan_layout(R, P, _i64_array(rows), _i64_array(row_len), m, s, o,
+                                  ctypes.byref(S), ctypes.byref(U)), "tide_plan_layout")
+    return list(m), list(s), list(o), S.value, U.value
+
+
+def tide_group_create(R: int, rows: Sequence[int], row_len: Sequence[int], flags: int = 0) -> int:
+    h = ctypes.c_void_p()
+    _check(lib().tide_group_create(ctypes.byref(h), R, len(rows), _i64_array(rows), _i64_array(row_len), flags),
+           "tide_group_create")
+    return h.value
+
+
+def tide_group_destroy(g: int) -> None:
+    _check(lib().tide_group_destroy(g), "tide_group_destroy")
+
+
+def tide_group_shard_elems(g: int) -> int:
+    v = ctypes.c_int64()
+    _check(lib().tide_group_shard_elems(g, ctypes.byref(v)), "tide_group_shard_elems")
+    return v.value
+
+
+def tide_group_unsharded_elems(g: int) -> int:
+    v = ctypes.c_int64()
+    _check(lib().tide_group_unsharded_elems(g, ctypes.byref(v)), "tide_group_unsharded_elems")
+    return v.value
+
+
+def tide_group_param_layout(g: int, p: int) -> Tuple[int, int]:
+    m, o = ctypes.c_int64(), ctypes.c_int64()
+    _check(lib().tide_group_param_layout(g, p, ctypes.byref(m), ctypes.byref(o)), "tide_group_param_layout")
+    return m.value, o.value
+
+
+def tide_group_valid_rows(g: int, d: int, p: int) -> int:
+    v = ctypes.c_int64()
+    _check(lib().tide_group_valid_rows(g, d, p, ctypes.byref(v)), "tide_group_valid_rows")
+    return v.value
+
+
+def tide_group_set_ctas(g: int, rs_ctas: int = 0, ag_ctas: int = 0) -> None:
+    _check(lib().tide_group_set_ctas(g, rs_ctas, ag_ctas), "tide_group_set_ctas")
+
+
+def tide_group_get_ctas(g: int) -> Tuple[int, int]:
+    a, b = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().tide_group_get_ctas(g, ctypes.byref(a), ctypes.byref(b)), "tide_group_get_ctas")
+    return a.value, b.value
+
+
+def _flat_grads(grads) -> List:
+    if len(grads) and isinstance(grads[0], (list, tuple)):
+        return [x for row in grads for x in row]
+    return list(grads)
+
+
+def tide_reduce_scatter(g: int, grads, shards: Sequence, stream=None) -> None:
+    """``grads``: R lists of P bf16 tensors (or a flat list indexed r*P+p, or raw pointers);
+    ``shards``: R fp32 tensors of at least S elements."""
+    _check(lib().tide_reduce_scatter(g, _ptr_array(_flat_grads(grads)), _ptr_array(shards), _stream(stream)),
+           "tide_reduce_scatter")
+
+
+def tide_all_gather(g: int, shards: Sequence, params: Sequence, stream=None) -> None:
+    _check(lib().tide_all_gather(g, _ptr_array(shards), _ptr_array(params), _stream(stream)), "tide_all_gather")
+
+
+def tide_all_gather_ce(g: int, shards: Sequence, params: Sequence, stream=None) -> None:
+    _check(lib().tide_all_gather_ce(g, _ptr_array(shards), _ptr_array(params), _stream(stream)),
+           "tide_all_gather_ce")
+
+
+def tide_group_last_ce_copies(g: int) -> Tuple[int, bool]:
+    n, u = ctypes.c_int64(), ctypes.c_int32()
+    _check(lib().tide_group_last_ce_copies(g, ctypes.byref(n), ctypes.byref(u)), "tide_group_last_ce_copies")
+    return n.value, bool(u.value)
+
+
+# ---- convenience object -----------------------------------------------------------------------
+
+
+class Group:
+    """Owns one ``tide_group_t``.  ``params`` is a list of ``(rows, row_len)`` pairs."""
+
+    def __init__(self, R: int, params: Sequence[Tuple[int, int]], flags: int = 0):
+        self.R = R
+        self.rows = [int(r) for r, _ in params]
+        self.row_len = [int(l) for _, l in params]
+        self.P = len(self.rows)
+        self.handle = tide_group_create(R, self.rows, self.row_len, flags)
+        self.S = tide_group_shard_elems(self.handle)
+        self.U = tide_group_unsharded_elems(self.handle)
+
+    def close(self) -> None:
+        if self.handle:
+            tide_group_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def param_layout(self, p: int) -> Tuple[int, int]:
+        return tide_group_param_layout(self.handle, p)
+
+    def valid_rows(self, d: int, p: int) -> int:
+        return tide_group_valid_rows(self.handle, d, p)
+
+    def set_ctas(self, rs_ctas: int = 0, ag_ctas: int = 0) -> None:
+        tide_group_set_ctas(self.handle, rs_ctas, ag_ctas)
+
+    def get_ctas(self) -> Tuple[int, int]:
+        return tide_group_get_ctas(self.handle)
+
+    def reduce_scatter(self, grads, shards, stream=None) -> None:
+        tide_reduce_scatter(self.handle, grads, shards, stream)
+
+    def all_gather(self, shards, params, stream=None) -> None:
+        tide_all_gather(self.handle, shards, params, stream)
+
+    def all_gather_ce(self, shards, params, stream=None) -> None:
+        tide_all_gather_ce(self.handle, shards, params, stream)
+
+    def last_ce_copies(self) -> Tuple[int, bool]:
+        return tide_group_last_ce_copies(self.handle)

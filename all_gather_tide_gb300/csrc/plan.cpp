@@ -1,0 +1,100 @@
+// Group planner: the per-parameter layout of Table 2 of the paper ("The Endgame of FSDP
+// Communication", arXiv 2610.38228) and the flat chunk lists the kernels walk.
+//
+// Layout (abstract; Fig. 1; Table 2): parameter p is split on dim 0 into R pieces of
+// m_p = ceil(rows_p / R) rows; a piece is s_p = m_p * L_p elements; the pieces of all parameters
+// are packed in parameter order at prefix offsets o_p into each rank's shard of S elements.
+// Because dim-0 pieces of a row-major tensor are contiguous, rank d's piece of p is the range
+// [d*s_p, d*s_p + v(d,p)*L_p) of the tensor, v(d,p) = clamp(rows_p - d*m_p, 0, m_p).
+#include <algorithm>
+
+#include "../../include/tide.h"
+#include "tide_internal.h"
+
+namespace tide {
+
+namespace {
+bool mul_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_mul_overflow(a, b, out); }
+bool add_ok(int64_t a, int64_t b, int64_t* out) { return !__builtin_add_overflow(a, b, out); }
+}  // namespace
+
+int64_t valid_rows(int64_t rows_p, int64_t m_p, int64_t d) {
+    return std::min(m_p, std::max<int64_t>(0, rows_p - d * m_p));
+}
+
+int make_layout(int32_t R, int32_t P, const int64_t* rows, const int64_t* row_len, Plan* out) {
+    if (!rows || !row_len || !out || R < 1 || R > TIDE_MAX_RANKS || P < 1) return TIDE_EINVAL;
+    Plan pl;
+    pl.R = R;
+    pl.P = P;
+    pl.rows.assign(rows, rows + P);
+    pl.row_len.assign(row_len, row_len + P);
+    pl.m.resize(P);
+    pl.s.resize(P);
+    pl.o.resize(P);
+    int64_t off = 0, un = 0;
+    for (int32_t p = 0; p < P; ++p) {
+        if (rows[p] < 1 || row_len[p] < 1) return TIDE_EINVAL;
+        const int64_t m = rows[p] / R + (rows[p] % R != 0);
+        int64_t s, n, Rm;
+        if (!mul_ok(m, row_len[p], &s) || !mul_ok(rows[p], row_len[p], &n) || !mul_ok(m, R, &Rm) ||
+            !mul_ok(Rm, row_len[p], &Rm))
+            return TIDE_ERANGE;
+        pl.m[p] = m;
+        pl.s[p] = s;
+        pl.o[p] = off;
+        if (!add_ok(off, s, &off) || !add_ok(un, n, &un)) return TIDE_ERANGE;
+    }
+    int64_t total;
+    if (!mul_ok(off, R, &total) || !mul_ok(total, 4, &total)) return TIDE_ERANGE;
+    pl.S = off;
+    pl.U = un;
+    *out = std::move(pl);
+    return TIDE_OK;
+}
+
+void make_work_lists(Plan* pl) {
+    // Reduce-scatter: destination-major, parameter order within a shard, so each CTA pass
+    // writes a contiguous run of the shard and reads R contiguous runs of gradient p.
+    pl->rs.clear();
+    int64_t chunks = 0;
+    for (int32_t d = 0; d < pl->R; ++d) {
+        for (int32_t p = 0; p < pl->P; ++p) {
+            RsSeg sg{};
+            sg.dst_off = pl->o[p];
+            sg.src_off = int64_t(d) * pl->s[p];
+            sg.valid = valid_rows(pl->rows[p], pl->m[p], d) * pl->row_len[p];
+            sg.total = pl->s[p];
+            sg.chunk_begin = chunks;
+            sg.d = d;
+            sg.p = p;
+            sg.vec = (sg.src_off % 8 == 0) && (sg.dst_off % 4 == 0);
+            chunks += (sg.total + kRsChunk - 1) / kRsChunk;
+            pl->rs.push_back(sg);
+        }
+    }
+    pl->rs_chunks = chunks;
+
+    // All-gather placement: source-rank-major runs of valid elements; padding never appears.
+    pl->ag.clear();
+    chunks = 0;
+    for (int32_t r = 0; r < pl->R; ++r) {
+        for (int32_t p = 0; p < pl->P; ++p) {
+            const int64_t len = valid_rows(pl->rows[p], pl->m[p], r) * pl->row_len[p];
+            if (len == 0) continue;
+            AgSeg sg{};
+            sg.src_off = pl->o[p];
+            sg.dst_off = int64_t(r) * pl->s[p];
+            sg.len = len;
+            sg.chunk_begin = chunks;
+            sg.r = r;
+            sg.p = p;
+            sg.vec = (sg.src_off % 8 == 0) && (sg.dst_off % 8 == 0);
+            chunks += (len + kAgChunk - 1) / kAgChunk;
+            pl->ag.push_back(sg);
+        }
+    }
+    pl->ag_chunks = chunks;
+}
+
+}  // namespace tide

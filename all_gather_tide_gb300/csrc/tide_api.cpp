@@ -1,0 +1,376 @@
+// C ABI of the library (declared in include/tide.h): argument checks, the group object, the
+// per-call pointer-table upload, kernel launches and the copy-engine placement path.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "../../include/tide.h"
+#include "tide_internal.h"
+
+namespace {
+
+constexpr int kSlots = 4;  // pointer-table ring depth
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = int(e);
+    return TIDE_ECUDA;
+}
+
+#define TIDE_CUDA(call)                                   \
+    do {                                                  \
+        cudaError_t e_ = (call);                          \
+        if (e_ != cudaSuccess) return cuda_fail(e_);      \
+    } while (0)
+
+// One entry of the ring of pointer tables.  The host copy is pinned so the upload is a true
+// asynchronous copy on the caller's stream; `done` is recorded after the kernel that reads the
+// device copy, so the slot is only rewritten once that kernel has finished.
+struct Slot {
+    std::vector<const void*> content;
+    const void** host = nullptr;
+    void** dev = nullptr;
+    cudaEvent_t done = nullptr;
+    cudaStream_t stream = nullptr;
+    uint64_t last_use = 0;
+    bool valid = false;
+    bool pending = false;
+};
+
+}  // namespace
+
+struct tide_group {
+    tide::Plan plan;
+    uint32_t flags = 0;
+    int device = 0;
+    int sm_count = 0;
+    int rs_ctas = 0, ag_ctas = 0;  // 0 = default
+    tide::RsSeg* d_rs = nullptr;
+    tide::AgSeg* d_ag = nullptr;
+    size_t slot_cap = 0;
+    Slot slots[kSlots];
+    uint64_t use_clock = 0;
+    int64_t last_ce_copies = 0;
+    int32_t last_ce_uniform = 0;
+    std::mutex mu;
+};
+
+namespace {
+
+void release(tide_group* g) {
+    if (!g) return;
+    for (Slot& s : g->slots) {
+        if (s.done) {
+            cudaEventSynchronize(s.done);
+            cudaEventDestroy(s.done);
+        }
+        if (s.host) cudaFreeHost(s.host);
+        if (s.dev) cudaFree(s.dev);
+    }
+    if (g->d_rs) cudaFree(g->d_rs);
+    if (g->d_ag) cudaFree(g->d_ag);
+    delete g;
+}
+
+int check_device(tide_group* g) {
+    int dev = -1;
+    TIDE_CUDA(cudaGetDevice(&dev));
+    return dev == g->device ? TIDE_OK : TIDE_EINVAL;
+}
+
+// Uploads `ptrs` into a ring slot (or finds a slot already holding the same table for the
+// same stream) and returns its index.  The caller records slots[k].done after its launch.
+int upload_table(tide_group* g, const std::vector<const void*>& ptrs, cudaStream_t stream, int* slot) {
+    for (int k = 0; k < kSlots; ++k) {
+        Slot& s = g->slots[k];
+        if (s.valid && s.stream == stream && s.content == ptrs) {
+            s.last_use = ++g->use_clock;
+            *slot = k;
+            return TIDE_OK;
+        }
+    }
+    // victim: an unused slot, else the least recently used one
+    int k = -1;
+    for (int i = 0; i < kSlots && k < 0; ++i)
+        if (!g->slots[i].valid) k = i;
+    if (k < 0) {
+        k = 0;
+        for (int i = 1; i < kSlots; ++i)
+            if (g->slots[i].last_use < g->slots[k].last_use) k = i;
+    }
+    Slot& s = g->slots[k];
+    if (s.pending) TIDE_CUDA(cudaEventSynchronize(s.done));
+    s.valid = false;
+    std::memcpy(s.host, ptrs.data(), ptrs.size() * sizeof(void*));
+    TIDE_CUDA(cudaMemcpyAsync(s.dev, s.host, ptrs.size() * sizeof(void*), cudaMemcpyHostToDevice, stream));
+    s.content = ptrs;
+    s.stream = stream;
+    s.valid = true;
+    s.last_use = ++g->use_clock;
+    *slot = k;
+    return TIDE_OK;
+}
+
+int finish_slot(tide_group* g, int k, cudaStream_t stream) {
+    Slot& s = g->slots[k];
+    TIDE_CUDA(cudaEventRecord(s.done, stream));
+    s.pending = true;
+    return TIDE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int default_ctas(const tide_group* g, int per_sm) { return std::max(1, g->sm_count * per_sm); }
+
+}  // namespace
+
+extern "C" {
+
+int tide_version(void) { return 100; }
+
+const char* tide_strerror(int status) {
+    switch (status) {
+        case TIDE_OK: return "success";
+        case TIDE_EINVAL: return "invalid argument";
+        case TIDE_EALIGN: return "pointer not 16-byte aligned (TIDE_FLAG_VEC_STRICT)";
+        case TIDE_ELAYOUT: return "shards not at a uniform pitch (TIDE_FLAG_CE_STRICT)";
+        case TIDE_ECUDA: return "CUDA runtime error (see tide_last_cuda_error)";
+        case TIDE_ENOMEM: return "out of memory";
+        case TIDE_ERANGE: return "size out of range";
+        default: return "unknown status";
+    }
+}
+
+int tide_last_cuda_error(void) { return g_last_cuda_error; }
+
+int tide_plan_layout(int32_t R, int32_t P, const int64_t* rows, const int64_t* row_len, int64_t* m,
+                     int64_t* s, int64_t* o, int64_t* S, int64_t* U) {
+    if (!m || !s || !o || !S || !U) return TIDE_EINVAL;
+    tide::Plan pl;
+    const int rc = tide::make_layout(R, P, rows, row_len, &pl);
+    if (rc != TIDE_OK) return rc;
+    std::copy(pl.m.begin(), pl.m.end(), m);
+    std::copy(pl.s.begin(), pl.s.end(), s);
+    std::copy(pl.o.begin(), pl.o.end(), o);
+    *S = pl.S;
+    *U = pl.U;
+    return TIDE_OK;
+}
+
+int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* rows, const int64_t* row_len,
+                      uint32_t flags) {
+    if (!out) return TIDE_EINVAL;
+    *out = nullptr;
+    tide::Plan pl;
+    int rc = tide::make_layout(R, P, rows, row_len, &pl);
+    if (rc != TIDE_OK) return rc;
+    if (int64_t(R) * P > TIDE_MAX_TABLE) return TIDE_ERANGE;
+    tide::make_work_lists(&pl);
+
+    tide_group* g = new (std::nothrow) tide_group();
+    if (!g) return TIDE_ENOMEM;
+    g->plan = std::move(pl);
+    g->flags = flags;
+    cudaError_t e = cudaGetDevice(&g->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g->sm_count, cudaDevAttrMultiProcessorCount, g->device);
+    if (e != cudaSuccess) {
+        release(g);
+        return cuda_fail(e);
+    }
+    const auto& rs = g->plan.rs;
+    const auto& ag = g->plan.ag;
+    e = cudaMalloc(&g->d_rs, std::max<size_t>(1, rs.size()) * sizeof(tide::RsSeg));
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_ag, std::max<size_t>(1, ag.size()) * sizeof(tide::AgSeg));
+    if (e == cudaSuccess && !rs.empty())
+        e = cudaMemcpy(g->d_rs, rs.data(), rs.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !ag.empty())
+        e = cudaMemcpy(g->d_ag, ag.data(), ag.size() * sizeof(tide::AgSeg), cudaMemcpyHostToDevice);
+    // a table holds the R*P gradient pointers + R shard pointers (reduce-scatter) or R + P
+    // pointers (all-gather)
+    g->slot_cap = size_t(R) * P + R + P;
+    for (Slot& s : g->slots) {
+        if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&s.host), g->slot_cap * sizeof(void*), cudaHostAllocDefault);
+        if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s.dev), g->slot_cap * sizeof(void*));
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+        release(g);
+        return e == cudaErrorMemoryAllocation ? (g_last_cuda_error = int(e), TIDE_ENOMEM) : cuda_fail(e);
+    }
+    *out = g;
+    return TIDE_OK;
+}
+
+int tide_group_destroy(tide_group_t g) {
+    if (!g) return TIDE_OK;
+    release(g);
+    return TIDE_OK;
+}
+
+int tide_group_shard_elems(tide_group_t g, int64_t* S) {
+    if (!g || !S) return TIDE_EINVAL;
+    *S = g->plan.S;
+    return TIDE_OK;
+}
+
+int tide_group_unsharded_elems(tide_group_t g, int64_t* U) {
+    if (!g || !U) return TIDE_EINVAL;
+    *U = g->plan.U;
+    return TIDE_OK;
+}
+
+int tide_group_param_layout(tide_group_t g, int32_t p, int64_t* m_p, int64_t* o_p) {
+    if (!g || !m_p || !o_p || p < 0 || p >= g->plan.P) return TIDE_EINVAL;
+    *m_p = g->plan.m[p];
+    *o_p = g->plan.o[p];
+    return TIDE_OK;
+}
+
+int tide_group_valid_rows(tide_group_t g, int32_t d, int32_t p, int64_t* v) {
+    if (!g || !v || p < 0 || p >= g->plan.P || d < 0 || d >= g->plan.R) return TIDE_EINVAL;
+    *v = tide::valid_rows(g->plan.rows[p], g->plan.m[p], d);
+    return TIDE_OK;
+}
+
+int tide_group_set_ctas(tide_group_t g, int32_t rs_ctas, int32_t ag_ctas) {
+    if (!g || rs_ctas < 0 || ag_ctas < 0) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    g->rs_ctas = rs_ctas;
+    g->ag_ctas = ag_ctas;
+    return TIDE_OK;
+}
+
+int tide_group_get_ctas(tide_group_t g, int32_t* rs_ctas, int32_t* ag_ctas) {
+    if (!g || !rs_ctas || !ag_ctas) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    *rs_ctas = g->rs_ctas ? g->rs_ctas : default_ctas(g, tide::kRsCtasPerSm);
+    *ag_ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgCtasPerSm);
+    return TIDE_OK;
+}
+
+int tide_reduce_scatter(tide_group_t g, const void* const* grads, void* const* shards, void* stream) {
+    if (!g || !grads || !shards) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    const int R = g->plan.R, P = g->plan.P;
+    std::vector<const void*> table(size_t(R) * P + R);
+    bool aligned = true;
+    for (size_t i = 0; i < size_t(R) * P; ++i) {
+        if (!grads[i]) return TIDE_EINVAL;
+        table[i] = grads[i];
+        aligned &= aligned16(grads[i]);
+    }
+    for (int d = 0; d < R; ++d) {
+        if (!shards[d]) return TIDE_EINVAL;
+        table[size_t(R) * P + d] = shards[d];
+        aligned &= aligned16(shards[d]);
+    }
+    if (!aligned && (g->flags & TIDE_FLAG_VEC_STRICT)) return TIDE_EALIGN;
+    int rc = check_device(g);
+    if (rc != TIDE_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int k = 0;
+    if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
+    void** dev = g->slots[k].dev;
+    const int ctas = g->rs_ctas ? g->rs_ctas : default_ctas(g, tide::kRsCtasPerSm);
+    const cudaError_t e = tide::launch_reduce_scatter(
+        g->d_rs, int(g->plan.rs.size()), g->plan.rs_chunks, reinterpret_cast<const uint16_t* const*>(dev),
+        reinterpret_cast<float* const*>(dev + size_t(R) * P), R, P, aligned ? 1 : 0, ctas, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return finish_slot(g, k, st);
+}
+
+int tide_all_gather(tide_group_t g, const void* const* shards, void* const* params, void* stream) {
+    if (!g || !shards || !params) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    const int R = g->plan.R, P = g->plan.P;
+    std::vector<const void*> table(size_t(R) + P);
+    bool aligned = true;
+    for (int r = 0; r < R; ++r) {
+        if (!shards[r]) return TIDE_EINVAL;
+        table[r] = shards[r];
+        aligned &= aligned16(shards[r]);
+    }
+    for (int p = 0; p < P; ++p) {
+        if (!params[p]) return TIDE_EINVAL;
+        table[size_t(R) + p] = params[p];
+        aligned &= aligned16(params[p]);
+    }
+    if (!aligned && (g->flags & TIDE_FLAG_VEC_STRICT)) return TIDE_EALIGN;
+    int rc = check_device(g);
+    if (rc != TIDE_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int k = 0;
+    if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
+    void** dev = g->slots[k].dev;
+    const int ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgCtasPerSm);
+    const cudaError_t e = tide::launch_all_gather(
+        g->d_ag, int(g->plan.ag.size()), g->plan.ag_chunks, reinterpret_cast<const uint16_t* const*>(dev),
+        reinterpret_cast<uint16_t* const*>(dev + R), aligned ? 1 : 0, ctas, st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return finish_slot(g, k, st);
+}
+
+int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* params, void* stream) {
+    if (!g || !shards || !params) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    const tide::Plan& pl = g->plan;
+    const int R = pl.R, P = pl.P;
+    for (int r = 0; r < R; ++r)
+        if (!shards[r]) return TIDE_EINVAL;
+    for (int p = 0; p < P; ++p)
+        if (!params[p]) return TIDE_EINVAL;
+    // Uniform pitch: shards[r] = shards[0] + r * pitch with pitch >= S*2 bytes.
+    const char* base = static_cast<const char*>(shards[0]);
+    const int64_t pitch = R > 1 ? static_cast<const char*>(shards[1]) - base : pl.S * 2;
+    bool uniform = pitch >= pl.S * 2;
+    for (int r = 1; r < R && uniform; ++r) uniform = static_cast<const char*>(shards[r]) == base + int64_t(r) * pitch;
+    if (!uniform && (g->flags & TIDE_FLAG_CE_STRICT)) return TIDE_ELAYOUT;
+    int rc = check_device(g);
+    if (rc != TIDE_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int64_t copies = 0;
+    for (int p = 0; p < P; ++p) {
+        char* dst = static_cast<char*>(params[p]);
+        const int64_t piece_bytes = pl.s[p] * 2;
+        if (uniform) {
+            // ranks 0 .. f-1 hold full pieces of m_p rows: one 2-D copy, source rows `pitch`
+            // apart, destination rows contiguous
+            const int64_t f = pl.rows[p] / pl.m[p];
+            if (f > 0) {
+                TIDE_CUDA(cudaMemcpy2DAsync(dst, size_t(piece_bytes), base + pl.o[p] * 2, size_t(pitch),
+                                            size_t(piece_bytes), size_t(f), cudaMemcpyDeviceToDevice, st));
+                ++copies;
+            }
+            const int64_t rest = pl.rows[p] - f * pl.m[p];
+            if (rest > 0) {
+                TIDE_CUDA(cudaMemcpyAsync(dst + f * piece_bytes, base + f * pitch + pl.o[p] * 2,
+                                          size_t(rest * pl.row_len[p] * 2), cudaMemcpyDeviceToDevice, st));
+                ++copies;
+            }
+        } else {
+            for (int r = 0; r < R; ++r) {
+                const int64_t v = tide::valid_rows(pl.rows[p], pl.m[p], r);
+                if (v == 0) continue;
+                TIDE_CUDA(cudaMemcpyAsync(dst + r * piece_bytes, static_cast<const char*>(shards[r]) + pl.o[p] * 2,
+                                          size_t(v * pl.row_len[p] * 2), cudaMemcpyDeviceToDevice, st));
+                ++copies;
+            }
+        }
+    }
+    g->last_ce_copies = copies;
+    g->last_ce_uniform = uniform ? 1 : 0;
+    return TIDE_OK;
+}
+
+int tide_group_last_ce_copies(tide_group_t g, int64_t* copies, int32_t* uniform_pitch) {
+    if (!g || !copies || !uniform_pitch) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    *copies = g->last_ce_copies;
+    *uniform_pitch = g->last_ce_uniform;
+    return TIDE_OK;
+}
+
+}  // extern "C"

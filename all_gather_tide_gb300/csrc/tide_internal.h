@@ -1,0 +1,73 @@
+// Internal declarations shared by the host side of the library and its kernels.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+namespace tide {
+
+// Reduce-scatter kernel geometry: a chunk is the work of one CTA pass, kRsUnroll 16-byte
+// bf16 vectors (8 elements) per thread.
+constexpr int kRsThreads = 256;
+constexpr int kRsUnroll = 2;
+constexpr int64_t kRsChunk = int64_t(kRsThreads) * 8 * kRsUnroll;  // 4096 elements
+constexpr int kRsCtasPerSm = 2;
+
+// All-gather placement kernel geometry.
+constexpr int kAgThreads = 256;
+constexpr int kAgUnroll = 4;
+constexpr int64_t kAgChunk = int64_t(kAgThreads) * 8 * kAgUnroll;  // 8192 elements
+constexpr int kAgCtasPerSm = 4;
+
+// One (destination rank d, parameter p) piece of the reduce-scatter output.
+struct RsSeg {
+    int64_t dst_off;      // o_p: element offset of the piece in shard d
+    int64_t src_off;      // d*s_p: element offset of the piece in every rank's gradient of p
+    int64_t valid;        // v(d,p)*L_p: elements that are sums; the rest of the piece is padding
+    int64_t total;        // s_p
+    int64_t chunk_begin;  // index of the piece's first chunk in the flat chunk list
+    int32_t d, p;
+    int32_t vec;  // both offsets allow 16-byte vectors (src_off % 8 == 0, dst_off % 4 == 0)
+    int32_t pad_;
+};
+static_assert(sizeof(RsSeg) == 56, "RsSeg layout");
+
+// One (source rank r, parameter p) run of valid elements for the all-gather placement.
+struct AgSeg {
+    int64_t src_off;      // o_p: element offset in shard r
+    int64_t dst_off;      // r*s_p: element offset in parameter p
+    int64_t len;          // v(r,p)*L_p
+    int64_t chunk_begin;  // index of the run's first chunk in the flat chunk list
+    int32_t r, p;
+    int32_t vec;  // both offsets are multiples of 8 elements
+    int32_t pad_;
+};
+static_assert(sizeof(AgSeg) == 48, "AgSeg layout");
+
+// Group layout (Table 2 of the paper) and the flat work lists built from it.
+struct Plan {
+    int32_t R = 0, P = 0;
+    std::vector<int64_t> rows, row_len, m, s, o;
+    int64_t S = 0, U = 0;
+    std::vector<RsSeg> rs;
+    int64_t rs_chunks = 0;
+    std::vector<AgSeg> ag;
+    int64_t ag_chunks = 0;
+};
+
+// Returns 0 or a negative TIDE_* status.
+int make_layout(int32_t R, int32_t P, const int64_t* rows, const int64_t* row_len, Plan* out);
+void make_work_lists(Plan* plan);
+int64_t valid_rows(int64_t rows_p, int64_t m_p, int64_t d);
+
+// Kernel launchers (stream-ordered; return the launch status).
+cudaError_t launch_reduce_scatter(const RsSeg* segs, int nsegs, int64_t nchunks,
+                                  const uint16_t* const* grads, float* const* shards, int R, int P,
+                                  int allow_vec, int ctas, cudaStream_t stream);
+cudaError_t launch_all_gather(const AgSeg* segs, int nsegs, int64_t nchunks,
+                              const uint16_t* const* shards, uint16_t* const* params,
+                              int allow_vec, int ctas, cudaStream_t stream);
+
+}  // namespace tide

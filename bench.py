@@ -1,0 +1,557 @@
+"""Benchmark of the layout-aware reduce-scatter + all-gather placement on one GB300 per process.
+
+A step is one pass of the hot path over one batch of synthetic input: the mixed-precision
+reduce-scatter of a whole parameter group (R ranks' bf16 gradients -> R fp32 shards) followed by
+the all-gather placement of R packed bf16 shards into per-parameter storage (SM kernel).  The
+default workload is the Llama-3.1-70B decoder-layer group at R = 8.  Inputs are resident in HBM
+and larger than L2 (17.1 GB of reduce-scatter traffic per step), so no L2 flush is needed.
+
+Printed (rank 0, one JSON line): the effective HBM GB/s of the step (algorithmic bytes / time),
+per-leg GB/s and fraction of the measured HBM peak (reduce-scatter, SM placement, copy-engine
+placement), the roofline of the dominant kernel (reduce-scatter), the end-to-end figure through
+the C ABI with host buffers, the slowdown of a concurrent single-wave cuBLAS bf16 GEMM
+(4096 x 4096 x 8192) on another stream, SM clocks sampled during the timed region, and the CPU
+oracle timed on the host on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tide|reference] [--workload NAME]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import Group, group, rng  # noqa: E402
+
+METRIC = "RS/AG effective HBM GB/s and % of GB300 peak; concurrent GEMM slowdown %"
+FALLBACK_HBM_GBS = 6800.0
+# Bounded sample of the workload for the host-side oracle: these parameters of the group.
+CPU_SAMPLE_PARAMS = ("k", "v", "o", "input_norm", "post_norm")
+
+
+def workload(args) -> Group:
+    g = group(args.workload)
+    return g.scaled(args.scale) if args.scale > 1 else g
+
+
+# ---- layout arithmetic for the byte counts (through the library's host-only planner) ---------
+
+
+def layout(g: Group):
+    import all_gather_tide_gb300 as tide
+
+    m, s, o, S, U = tide.tide_plan_layout(g.R, g.rows, g.row_len)
+    return S, U
+
+
+def rs_bytes(g: Group, S: int, U: int) -> int:
+    """Algorithmic reduce-scatter bytes: R*U*2 bf16 read + R*S*4 fp32 written (padding included)."""
+    return g.R * U * 2 + g.R * S * 4
+
+
+def ag_bytes(U: int) -> int:
+    """Algorithmic all-gather placement bytes: U*2 read + U*2 written (padding neither)."""
+    return 4 * U
+
+
+# ---- peaks, clocks, profiles -------------------------------------------------------------------
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "all_gather_tide_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str, srcs):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current source."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = rec.get(kernel, {}).get(workload)
+    if not e or e.get("source_hash") != kernel_source_hash(srcs):
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.samples = []
+        self.proc = None
+        self.uuid = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu=uuid,{self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        rows = self.samples
+        if self.uuid:
+            mine = [r for r in rows if self.uuid.replace("GPU-", "") in r[0]]
+            if mine:
+                rows = mine
+        sm = [float(r[1]) for r in rows if len(r) > 7 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) > 7 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows if len(r) > 7 for i in range(4) if r[4 + i] == "Active"})
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(sm)}
+
+
+# ---- multi-process aggregation (one replica per GPU; no data-path collective) ----------------
+
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """Slowest rank's elapsed time (ms); the identity at world size 1."""
+    if world <= 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Units all ranks processed / the slowest rank's time, in GB/s."""
+    return bytes_per_step * steps * world / (max_ms * 1e-3) / 1e9
+
+
+# ---- device buffers ----------------------------------------------------------------------------
+
+
+class Buffers:
+    def __init__(self, g: Group, S: int, device):
+        self.grads = [[rng.grad_bits(g, r, p, device=device).view(torch.bfloat16) for p in range(g.P)]
+                      for r in range(g.R)]
+        self.shards = torch.empty(g.R, S, dtype=torch.float32, device=device)
+        self.ag_in = torch.stack([rng.shard_bits(g, r, S, device=device) for r in range(g.R)]).view(torch.bfloat16)
+        self.params = [torch.empty(g.numel(p), dtype=torch.bfloat16, device=device) for p in range(g.P)]
+        self.shard_list = list(self.shards)
+        self.ag_list = list(self.ag_in)
+
+
+# ---- the GPU arm -------------------------------------------------------------------------------
+
+
+def run_tide(args, rank, world, local_rank):
+    import all_gather_tide_gb300 as tide
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    g = workload(args)
+    S, U = layout(g)
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+    G.set_ctas(args.rs_ctas, args.ag_ctas)
+    rs_ctas, ag_ctas = G.get_ctas()
+    buf = Buffers(g, S, dev)
+    stream = torch.cuda.Stream(device=dev)
+    b_rs, b_ag = rs_bytes(g, S, U), ag_bytes(U)
+    peak, peak_kind = hbm_peak()
+
+    def step(ce=False):
+        G.reduce_scatter(buf.grads, buf.shard_list, stream)
+        (G.all_gather_ce if ce else G.all_gather)(buf.ag_list, buf.params, stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+
+    # -- timed region: K steps, events on the launching stream around every kernel -------------
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        with torch.cuda.stream(stream):
+            for k in range(args.steps):
+                ev[k][0].record(stream)
+                G.reduce_scatter(buf.grads, buf.shard_list, stream)
+                ev[k][1].record(stream)
+                G.all_gather(buf.ag_list, buf.params, stream)
+                ev[k][2].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = max_over_ranks(ev[0][0].elapsed_time(ev[-1][2]), world, dev)
+    rs_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    ag_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    ms_per_step = total_ms / args.steps
+    step_bytes = b_rs + b_ag
+    value = whole_job_gbs(step_bytes, args.steps, world, total_ms)
+
+    rs_avg = statistics.mean(rs_ms)
+    ag_avg = statistics.mean(ag_ms)
+    legs = {
+        "reduce_scatter": {"gbs": b_rs / (rs_avg * 1e-3) / 1e9, "ms": rs_avg, "ms_median": statistics.median(rs_ms),
+                           "bytes": b_rs, "ctas": rs_ctas},
+        "all_gather_sm": {"gbs": b_ag / (ag_avg * 1e-3) / 1e9, "ms": ag_avg, "ms_median": statistics.median(ag_ms),
+                          "bytes": b_ag, "ctas": ag_ctas},
+    }
+    # copy-engine placement, same buffers (outside the step's timed region)
+    legs["all_gather_ce"] = time_ce(G, buf, stream, b_ag, max(3, args.steps))
+    for leg in legs.values():
+        leg["frac_of_peak"] = leg["gbs"] / peak
+
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "io_dtypes": {"grads": "bf16", "rs_shards": "f32", "ag_shards": "bf16", "params": "bf16"},
+        "data": "synthetic (seeded counter-based N(0,1e-3) gradients, N(0,0.02) shards; layer shapes only)",
+        "config": {"workload": g.name, "R": g.R, "P": g.P, "U": U, "S": S,
+                   "step": "reduce_scatter + all_gather (SM kernel)",
+                   "step_bytes": step_bytes, "rs_ctas": rs_ctas, "ag_ctas": ag_ctas,
+                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.1f} GB of traffic per step), no flush",
+                   "replicas": world},
+        "legs": legs,
+        "gpu_launches": 2 * args.steps,
+    }
+    traffic = recorded_traffic("reduce_scatter_kernel", g.name, ["rs_kernel.cu", "tide_internal.h"])
+    out["roofline"] = {"bound": "hbm", "kernel": "reduce_scatter_kernel", "achieved": legs["reduce_scatter"]["gbs"],
+                       "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                       "frac": legs["reduce_scatter"]["gbs"] / peak, "traffic": traffic,
+                       "algorithmic_bytes": b_rs}
+    out["clocks"] = clocks.summary()
+
+    if not args.no_interference and rank == 0:
+        out["interference"] = interference(G, buf, stream, dev, args)
+    if not args.no_e2e:
+        out["e2e"] = end_to_end(G, g, buf, S, U, dev, args, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(g, dev, reps=args.cpu_reps)
+    G.close()
+    return out
+
+
+def time_ce(G, buf, stream, b_ag, iters):
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            G.all_gather_ce(buf.ag_list, buf.params, stream)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(iters)]
+        for e in ev:
+            e[0].record(stream)
+            G.all_gather_ce(buf.ag_list, buf.params, stream)
+            e[1].record(stream)
+    torch.cuda.synchronize()
+    ms = [e[0].elapsed_time(e[1]) for e in ev]
+    copies, uniform = G.last_ce_copies()
+    avg = statistics.mean(ms)
+    return {"gbs": b_ag / (avg * 1e-3) / 1e9, "ms": avg, "ms_median": statistics.median(ms), "bytes": b_ag,
+            "copies": copies, "uniform_pitch": uniform, "ctas": 0}
+
+
+# ---- interference harness ----------------------------------------------------------------------
+
+
+def interference(G, buf, stream, dev, args):
+    """Slowdown of a single-wave cuBLAS bf16 GEMM (M=N=4096, K=8192) run on a second stream
+    while a collective runs: median(GEMM time inside the collective) / median(alone) - 1."""
+    M = N = 4096
+    K = 8192
+    a = torch.randn(M, K, device=dev, dtype=torch.bfloat16)
+    b = torch.randn(K, N, device=dev, dtype=torch.bfloat16)
+    c = torch.empty(M, N, device=dev, dtype=torch.bfloat16)
+    gs = torch.cuda.Stream(device=dev)
+
+    def gemm():
+        torch.matmul(a, b, out=c)
+
+    with torch.cuda.stream(gs):
+        for _ in range(10):
+            gemm()
+        alone_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(50)]
+        for e in alone_ev:
+            e[0].record(gs)
+            gemm()
+            e[1].record(gs)
+    torch.cuda.synchronize()
+    alone = [e[0].elapsed_time(e[1]) for e in alone_ev]
+    t_alone = statistics.median(alone)
+
+    def concurrent(launch, label, reps=4):
+        inside = []
+        coll_ms = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            with torch.cuda.stream(stream):
+                launch()
+            s1.record(stream)
+            gs.wait_event(s0)
+            n = 64
+            ge = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+            with torch.cuda.stream(gs):
+                for e in ge:
+                    e[0].record(gs)
+                    gemm()
+                    e[1].record(gs)
+            torch.cuda.synchronize()
+            end = s0.elapsed_time(s1)
+            coll_ms.append(end)
+            for e in ge:
+                st, en = s0.elapsed_time(e[0]), s0.elapsed_time(e[1])
+                if st >= 0 and en <= end:
+                    inside.append(e[0].elapsed_time(e[1]))
+        res = {"collective_ms": statistics.median(coll_ms), "gemms_inside": len(inside)}
+        if inside:
+            res["gemm_ms"] = statistics.median(inside)
+            res["slowdown_pct"] = 100.0 * (statistics.median(inside) / t_alone - 1.0)
+        else:
+            res["slowdown_pct"] = None
+        return res
+
+    out = {"gemm": {"M": M, "N": N, "K": K, "dtype": "bf16", "alone_ms": t_alone,
+                    "tflops": 2 * M * N * K / (t_alone * 1e-3) / 1e12, "library": "cuBLAS via torch.matmul"}}
+    rs_default, ag_default = G.get_ctas()
+    out["reduce_scatter"] = dict(ctas=rs_default, **concurrent(lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream), "rs"))
+    for c in args.interference_ctas:
+        G.set_ctas(c, 0)
+        out[f"reduce_scatter_ctas{c}"] = dict(ctas=c, **concurrent(
+            lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream), "rs"))
+    G.set_ctas(args.rs_ctas, args.ag_ctas)
+    # the placement is short; run it several times back to back so GEMMs fit inside
+    out["all_gather_sm"] = dict(ctas=ag_default, **concurrent(
+        lambda: [G.all_gather(buf.ag_list, buf.params, stream) for _ in range(8)], "ag"))
+    out["all_gather_ce"] = dict(ctas=0, **concurrent(
+        lambda: [G.all_gather_ce(buf.ag_list, buf.params, stream) for _ in range(8)], "ce"))
+    return out
+
+
+# ---- end to end with host buffers --------------------------------------------------------------
+
+
+def end_to_end(G, g, buf, S, U, dev, args, world):
+    """Same step through the public API, with the inputs copied in from pinned host memory and
+    the outputs copied back every step, inside the timed region."""
+    h_grads = [[t.to("cpu").pin_memory() for t in row] for row in buf.grads]
+    h_ag = buf.ag_in.to("cpu").pin_memory()
+    h_shards = torch.empty(g.R, S, dtype=torch.float32).pin_memory()
+    h_params = [torch.empty(g.numel(p), dtype=torch.bfloat16).pin_memory() for p in range(g.P)]
+    stream = torch.cuda.Stream(device=dev)
+    h2d = sum(t.numel() * 2 for row in h_grads for t in row) + h_ag.numel() * 2
+    d2h = h_shards.numel() * 4 + sum(t.numel() * 2 for t in h_params)
+
+    def step():
+        for r in range(g.R):
+            for p in range(g.P):
+                buf.grads[r][p].copy_(h_grads[r][p], non_blocking=True)
+        buf.ag_in.copy_(h_ag, non_blocking=True)
+        G.reduce_scatter(buf.grads, buf.shard_list, stream)
+        G.all_gather(buf.ag_list, buf.params, stream)
+        h_shards.copy_(buf.shards, non_blocking=True)
+        for p in range(g.P):
+            h_params[p].copy_(buf.params[p], non_blocking=True)
+
+    steps = max(2, min(args.steps, args.e2e_steps))
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            step()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    value = whole_job_gbs(rs_bytes(g, S, U) + ag_bytes(U), steps, world, ms)
+    del h_grads, h_ag, h_shards, h_params
+    return {"value": value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "ms_per_step": ms / steps,
+            "how": "pinned host -> device copies of all inputs, tide_reduce_scatter + tide_all_gather, "
+                   "device -> pinned host copies of all outputs, every step, one stream"}
+
+
+# ---- the host oracle ---------------------------------------------------------------------------
+
+
+def cpu_sample(g: Group):
+    params = tuple(p for p in g.params if p[0] in CPU_SAMPLE_PARAMS) or g.params[:1]
+    return Group(g.name + "-sample", g.R, params, g.grad_kind, g.grad_sigma, g.shard_sigma, g.grad_seed,
+                 g.grad_seed_per_rank, g.shard_seed_base)
+
+
+def cpu_inputs(sub: Group, S: int, dev):
+    where = dev if (dev is not None and torch.cuda.is_available()) else "cpu"
+    grads = [[rng.grad_bits(sub, r, p, device=where).cpu().numpy().view(np.uint16) for p in range(sub.P)]
+             for r in range(sub.R)]
+    shards = [rng.shard_bits(sub, r, S, device=where).cpu().numpy().view(np.uint16) for r in range(sub.R)]
+    return grads, shards
+
+
+def oracle_step(oracle, lay, grads, shards, params):
+    oracle.reduce_scatter(lay, grads)
+    oracle.all_gather(lay, shards, params)
+
+
+def cpu_baseline(g: Group, dev, reps: int = 4):
+    import oracle
+
+    sub = cpu_sample(g)
+    lay = oracle.plan(sub.R, sub.rows, sub.row_len)
+    grads, shards = cpu_inputs(sub, lay.S, dev)
+    params = [np.empty(sub.numel(p), np.uint16) for p in range(sub.P)]
+    nbytes = rs_bytes(sub, lay.S, lay.U) + ag_bytes(lay.U)
+    oracle_step(oracle, lay, grads, shards, params)  # warm
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(oracle, lay, grads, shards, params)
+    dt = time.perf_counter() - t0
+    return {"value": nbytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "seconds": dt,
+            "sample": f"{g.name} restricted to {', '.join(p[0] for p in sub.params)} "
+                      f"({lay.U} of the group's elements per rank-set; reduce-scatter + all-gather, "
+                      f"{reps} passes), single-threaded C oracle",
+            "host_cpus": os.cpu_count()}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, timed on the host cores on a bounded
+    sample of the same workload, under the same metric."""
+    import oracle
+
+    oracle.build()
+    g = workload(args)
+    sub = cpu_sample(g)
+    lay = oracle.plan(sub.R, sub.rows, sub.row_len)
+    dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
+    grads, shards = cpu_inputs(sub, lay.S, dev)
+    params = [np.empty(sub.numel(p), np.uint16) for p in range(sub.P)]
+    nbytes = rs_bytes(sub, lay.S, lay.U) + ag_bytes(lay.U)
+    for _ in range(args.warmup):
+        oracle_step(oracle, lay, grads, shards, params)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(oracle, lay, grads, shards, params)
+    dt = time.perf_counter() - t0
+    value = nbytes * args.steps / dt / 1e9
+    sample = (f"{g.name} restricted to {', '.join(p[0] for p in sub.params)}; each step = reduce-scatter + "
+              f"all-gather of that sample, single-threaded C oracle")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (same generator and workload shapes)",
+        "config": {"workload": g.name, "R": g.R, "P": g.P, "sample_params": [p[0] for p in sub.params],
+                   "step": "reduce_scatter + all_gather on the host oracle"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["tide", "reference"], default="tide")
+    ap.add_argument("--workload", default="llama70b")
+    ap.add_argument("--scale", type=int, default=1, help="divide every dimension by this (profiling cases)")
+    ap.add_argument("--rs-ctas", type=int, default=0)
+    ap.add_argument("--ag-ctas", type=int, default=0)
+    ap.add_argument("--interference-ctas", type=int, nargs="*", default=[16, 32])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-reps", type=int, default=4)
+    ap.add_argument("--no-interference", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from all_gather_tide_gb300 import build as _b
+
+    if not os.path.exists(_b.LIB):
+        raise SystemExit(f"{_b.LIB} is missing: run __graft_entry__.build() first")
+    out = run_tide(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,162 @@
+/*
+ * tide.h — C ABI of the GB300 (sm_103a) layout-aware reduce-scatter and all-gather placement.
+ *
+ * "TIDE" is the paper "The Endgame of FSDP Communication: Layout-Aware Collectives on Copy
+ * Engines, RDMA, and NVSwitch" (arXiv 2610.38228).  Citations below name its abstract, figures
+ * and tables.
+ *
+ * Model.  An FSDP2 parameter group holds P parameters; parameter p has rows_p rows (dim 0) of
+ * row_len_p = L_p elements (the product of its other dims; 1 for a 1-D tensor), row-major and
+ * contiguous.  It is sharded on dim 0 over R ranks (abstract; Fig. 1):
+ *     m_p = ceil(rows_p / R)                    padded rows per rank         (Table 2)
+ *     s_p = m_p * L_p                           per-rank shard elements      (Table 2)
+ *     o_p = s_0 + ... + s_{p-1}                 prefix offset in a shard     (Table 2)
+ *     S   = sum_p s_p,   U = sum_p rows_p*L_p   packed shard / unsharded     (Table 2)
+ *     v(d,p) = clamp(rows_p - d*m_p, 0, m_p)    valid rows of p on rank d (the rest is padding)
+ * Rank d's piece of p is the contiguous element range [d*s_p, d*s_p + v(d,p)*L_p) of the tensor,
+ * and it lives at elements [o_p, o_p + s_p) of rank d's packed shard, padding rows last.
+ * On one GPU the R ranks are R separate buffers in that GPU's memory.
+ *
+ * Conventions for every call:
+ *   - All sizes and offsets are elements (int64).  Returns TIDE_OK (0) or a negative status.
+ *   - Device pointers are plain CUDA device addresses on the device that was current when the
+ *     group was created; that device must be current at every call on the group.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Collective
+ *     calls are asynchronous and stream-ordered: they return once the work is enqueued.  Their
+ *     inputs must stay alive and unmodified, and their outputs untouched, until the stream has
+ *     executed the call.  Errors raised by the kernels themselves surface at the next
+ *     synchronisation of that stream; argument errors are returned before anything is enqueued.
+ *   - Host pointer arrays (grads, shards, params) are copied before the call returns.
+ *   - The caller owns every device buffer.  A group owns only its plan tables (device), a small
+ *     ring of pinned host / device pointer tables and CUDA events; tide_group_destroy frees them.
+ *   - A group may be used from several host threads; calls on one group are serialised.
+ *   - Inputs and outputs of one call must not overlap.  Nothing here traps on the device.
+ */
+#ifndef TIDE_H
+#define TIDE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------------------ */
+#define TIDE_OK 0
+#define TIDE_EINVAL (-1)  /* null pointer, R < 1, P < 1, rows < 1, row_len < 1, bad index, wrong device */
+#define TIDE_EALIGN (-2)  /* TIDE_FLAG_VEC_STRICT set and a pointer is not 16-byte aligned */
+#define TIDE_ELAYOUT (-3) /* TIDE_FLAG_CE_STRICT set and the shards are not at a uniform pitch */
+#define TIDE_ECUDA (-4)   /* a CUDA runtime call failed; tide_last_cuda_error() gives its code */
+#define TIDE_ENOMEM (-5)  /* host or device allocation of the group's own tables failed */
+#define TIDE_ERANGE (-6)  /* a size overflows int64, or R*P exceeds TIDE_MAX_TABLE */
+
+#define TIDE_MAX_RANKS 4096
+#define TIDE_MAX_TABLE (1 << 22) /* max R*P pointer-table entries */
+
+/* ---- group flags ------------------------------------------------------------------------- */
+/* Return TIDE_EALIGN instead of running the element-wise path when a pointer passed to
+ * tide_reduce_scatter / tide_all_gather is not 16-byte aligned. */
+#define TIDE_FLAG_VEC_STRICT 0x1u
+/* Return TIDE_ELAYOUT from tide_all_gather_ce instead of falling back to one 1-D copy per
+ * (rank, parameter) when shards[r] != shards[0] + r*pitch for one pitch >= S*2 bytes. */
+#define TIDE_FLAG_CE_STRICT 0x2u
+
+typedef struct tide_group *tide_group_t;
+
+/* ---- planner ----------------------------------------------------------------------------- */
+/*
+ * tide_plan_layout — the Table 2 quantities of a group, host only (no CUDA call).
+ * In:  R ranks, P parameters, rows[P] (dim 0), row_len[P] (product of the other dims).
+ * Out: m[P], s[P], o[P] (caller-allocated, P entries each), *S, *U, as defined above.
+ * Errors: TIDE_EINVAL (null, R < 1, R > TIDE_MAX_RANKS, P < 1, rows < 1, row_len < 1),
+ *         TIDE_ERANGE (a size overflows int64).  Outputs are untouched on error.
+ */
+int tide_plan_layout(int32_t R, int32_t P, const int64_t *rows, const int64_t *row_len,
+                     int64_t *m, int64_t *s, int64_t *o, int64_t *S, int64_t *U);
+
+/*
+ * tide_group_create — plan a group (abstract; Fig. 1; Table 2) and upload its work tables to
+ * the current device.  `flags` is a bitwise OR of TIDE_FLAG_*.  On success *out owns the plan;
+ * on error *out is set to NULL.
+ * Errors: as tide_plan_layout, plus TIDE_ERANGE (R*P > TIDE_MAX_TABLE), TIDE_ENOMEM, TIDE_ECUDA.
+ */
+int tide_group_create(tide_group_t *out, int32_t R, int32_t P, const int64_t *rows,
+                      const int64_t *row_len, uint32_t flags);
+
+/* Frees the group's tables after waiting for its own work in flight.  NULL is accepted. */
+int tide_group_destroy(tide_group_t g);
+
+/* Per-rank packed shard elements S / unsharded group elements U. */
+int tide_group_shard_elems(tide_group_t g, int64_t *S);
+int tide_group_unsharded_elems(tide_group_t g, int64_t *U);
+
+/* Padded per-rank rows m_p and prefix offset o_p of parameter p (0 <= p < P). */
+int tide_group_param_layout(tide_group_t g, int32_t p, int64_t *m_p, int64_t *o_p);
+
+/* Valid rows v(d,p) that rank d holds of parameter p. */
+int tide_group_valid_rows(tide_group_t g, int32_t d, int32_t p, int64_t *v);
+
+/*
+ * CTA counts of the reduce-scatter and all-gather kernels.  0 restores the default (enough
+ * CTAs to fill every SM); a positive value is used as given (at most the work's chunk count),
+ * so a caller can leave SMs to concurrent compute (Fig. 3, Fig. 4, Table 4).
+ */
+int tide_group_set_ctas(tide_group_t g, int32_t rs_ctas, int32_t ag_ctas);
+int tide_group_get_ctas(tide_group_t g, int32_t *rs_ctas, int32_t *ag_ctas);
+
+/* ---- collectives ------------------------------------------------------------------------- */
+/*
+ * tide_reduce_scatter — layout-aware mixed-precision reduce-scatter (abstract: TIDE-RS consumes
+ * per-parameter bf16 gradients directly and reduces them into fp32 shards; Table 1 "In-Place
+ * Read"; Fig. 2b step 5).  For every destination rank d and parameter p:
+ *     shard_d[o_p + i] = g_0[i'] + g_1[i'] + ... + g_{R-1}[i'],  i' = d*s_p + i,  i < v(d,p)*L_p
+ *     shard_d[o_p + i] = +0.0f                                   v(d,p)*L_p <= i < s_p
+ * where g_r is rank r's bf16 gradient of p, widened exactly to fp32 and added in ascending
+ * rank order with IEEE fp32 round-to-nearest-even adds (no FMA, no flush-to-zero).  The
+ * shards are overwritten, not accumulated into, and not averaged.
+ *   grads:  host array of R*P device pointers, entry [r*P + p] = rank r's bf16 gradient of p
+ *           (rows_p*L_p elements, row-major, contiguous).  Read only, never packed.
+ *   shards: host array of R device pointers, entry d = rank d's fp32 shard of S elements.
+ * 16-byte aligned pointers take the vectorised path; others take an element-wise path with the
+ * same results (or TIDE_EALIGN under TIDE_FLAG_VEC_STRICT).
+ */
+int tide_reduce_scatter(tide_group_t g, const void *const *grads, void *const *shards,
+                        void *stream);
+
+/*
+ * tide_all_gather — all-gather placement, SM kernel (abstract: TIDE-AG delivers shards
+ * directly to parameter storage; Fig. 1; Fig. 5b).  For every rank r and parameter p:
+ *     param_p[r*s_p + i] = shard_r[o_p + i]      for i < v(r,p)*L_p
+ * Padding elements of the shards are never read; nothing outside the params is written.
+ *   shards: host array of R device pointers, entry r = rank r's packed bf16 shard (S elements).
+ *   params: host array of P device pointers, entry p = bf16 parameter p (rows_p*L_p elements).
+ */
+int tide_all_gather(tide_group_t g, const void *const *shards, void *const *params,
+                    void *stream);
+
+/*
+ * tide_all_gather_ce — the same placement with copy engines and no SM kernel (Fig. 5b: one
+ * strided copy per parameter; Table 1 "AG SM budget 0").  When shards[r] = shards[0] + r*pitch
+ * for one pitch >= S*2 bytes, each parameter takes one cudaMemcpy2DAsync over its full ranks
+ * (height f_p = floor(rows_p/m_p), width s_p*2 bytes) plus at most one cudaMemcpyAsync for the
+ * rank holding its last partial piece.  Otherwise it falls back to one cudaMemcpyAsync per
+ * (rank, parameter) with valid rows (or returns TIDE_ELAYOUT under TIDE_FLAG_CE_STRICT).
+ */
+int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *params,
+                       void *stream);
+
+/* Copies issued by the last tide_all_gather_ce on g, and whether the uniform-pitch form was used. */
+int tide_group_last_ce_copies(tide_group_t g, int64_t *copies, int32_t *uniform_pitch);
+
+/* ---- errors ------------------------------------------------------------------------------ */
+const char *tide_strerror(int status);
+/* cudaError_t code of the last CUDA failure reported as TIDE_ECUDA on this host thread. */
+int tide_last_cuda_error(void);
+/* Library version as major*10000 + minor*100 + patch. */
+int tide_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TIDE_H */

@@ -195,3 +195,16 @@ def rs_points(lay: Layout, d: np.ndarray, j: np.ndarray,
         vals[valid] = acc
         out[sel] = vals
     return out
+
+
+def ag_points(lay: Layout, p: int, idx: np.ndarray):
+    """Where all-gather output ``param_p[idx]`` comes from: (source rank, element of its shard).
+
+    Element idx of parameter p lies in row idx // L_p; that row belongs to rank row // m_p,
+    at padded row row - rank*m_p of its piece, which starts at o_p in the rank's shard."""
+    idx = np.asarray(idx, np.int64)
+    L, m = int(lay.row_len[p]), int(lay.m[p])
+    row = idx // L
+    r = row // m
+    j = int(lay.o[p]) + (row - r * m) * L + idx % L
+    return r, j

@@ -319,3 +319,20 @@ ALL_PINS = [
     pin_ag_roundtrip,
     pin_rs_points,
 ]
+
+
+def pin_ag_points(seed: int = 9):
+    """Single-output all-gather source positions reproduce the full all-gather."""
+    for gi, (R, rows, row_len) in enumerate(random_groups(seed)):
+        lay = oracle.plan(R, rows, row_len)
+        shards = [random_bf16(seed * 100 + gi * 10 + r, lay.S, 0.02) for r in range(R)]
+        out = [np.full(rows[p] * row_len[p], SENTINEL_BF16, np.uint16) for p in range(len(rows))]
+        oracle.all_gather(lay, shards, out)
+        for p in range(len(rows)):
+            idx = np.arange(rows[p] * row_len[p])
+            r, j = oracle.ag_points(lay, p, idx)
+            got = np.array([shards[a][b] for a, b in zip(r, j)], np.uint16)
+            assert np.array_equal(got, out[p])
+
+
+ALL_PINS.append(pin_ag_points)

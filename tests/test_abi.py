@@ -1,0 +1,100 @@
+"""The C ABI library on the CPU: it builds, loads, exports every declared symbol, its host-only
+planner matches the oracle's on every workload, and argument checks fail before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from workloads import GROUPS, group
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def tide():
+    from all_gather_tide_gb300 import build
+
+    build.build()
+    import all_gather_tide_gb300 as t
+
+    t.lib()
+    return t
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "tide.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(tide_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_exports_every_declared_symbol(tide):
+    names = _declared_symbols()
+    assert len(names) >= 16
+    L = tide.lib()
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in tide.SIGNATURES, n
+    assert set(tide.SIGNATURES) == set(names)
+
+
+def test_version_and_strerror(tide):
+    assert tide.tide_version() == 100
+    for st in range(0, -7, -1):
+        assert tide.tide_strerror(st) and tide.tide_strerror(st) != "unknown status"
+    assert tide.tide_strerror(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("name", sorted(GROUPS))
+def test_planner_matches_oracle(tide, name):
+    g = group(name)
+    m, s, o, S, U = tide.tide_plan_layout(g.R, g.rows, g.row_len)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    assert m == lay.m.tolist() and s == lay.s.tolist() and o == lay.o.tolist()
+    assert (S, U) == (lay.S, lay.U)
+
+
+def test_planner_matches_oracle_random(tide):
+    import oracle_pins
+
+    for R, rows, row_len in oracle_pins.random_groups(11, 50):
+        m, s, o, S, U = tide.tide_plan_layout(R, rows, row_len)
+        lay = oracle.plan(R, rows, row_len)
+        assert m == lay.m.tolist() and s == lay.s.tolist() and o == lay.o.tolist() and (S, U) == (lay.S, lay.U)
+
+
+def _create_status(tide, R, rows, row_len, flags=0, out=True):
+    L = tide.lib()
+    h = ctypes.c_void_p()
+    arr = lambda xs: (ctypes.c_int64 * max(1, len(xs)))(*xs)
+    return L.tide_group_create(ctypes.byref(h) if out else None, R, len(rows), arr(rows), arr(row_len), flags)
+
+
+def test_create_rejects_bad_arguments_before_cuda(tide):
+    assert _create_status(tide, 0, [4], [4]) == tide.TIDE_EINVAL
+    assert _create_status(tide, 5000, [4], [4]) == tide.TIDE_EINVAL
+    assert _create_status(tide, 2, [0], [4]) == tide.TIDE_EINVAL
+    assert _create_status(tide, 2, [4], [-1]) == tide.TIDE_EINVAL
+    assert _create_status(tide, 2, [], []) == tide.TIDE_EINVAL
+    assert _create_status(tide, 2, [4], [4], out=False) == tide.TIDE_EINVAL
+    assert _create_status(tide, 2, [1 << 40], [1 << 30]) == tide.TIDE_ERANGE
+
+
+def test_plan_layout_rejects(tide):
+    with pytest.raises(tide.TideError) as e:
+        tide.tide_plan_layout(0, [1], [1])
+    assert e.value.status == tide.TIDE_EINVAL
+    with pytest.raises(tide.TideError) as e:
+        tide.tide_plan_layout(8, [1 << 62], [4])
+    assert e.value.status == tide.TIDE_ERANGE
+
+
+def test_null_group_calls(tide):
+    L = tide.lib()
+    arr = (ctypes.c_void_p * 1)(0)
+    for fn in ("tide_reduce_scatter", "tide_all_gather", "tide_all_gather_ce"):
+        assert getattr(L, fn)(None, arr, arr, None) == tide.TIDE_EINVAL
+    v = ctypes.c_int64()
+    assert L.tide_group_shard_elems(None, ctypes.byref(v)) == tide.TIDE_EINVAL
+    assert L.tide_group_destroy(None) == tide.TIDE_OK

@@ -1,0 +1,69 @@
+"""Host-side logic of the benchmark: whole-job aggregation over replicas (world size 2, gloo on
+the CPU), byte formulas, and the reference arm's JSON contract."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from workloads import group  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, out):
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    ms = [40.0, 55.5][rank]
+    m = bench.max_over_ranks(ms, world, "cpu")
+    dist.barrier()
+    out[rank] = m
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world2():
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    mgr = ctx.Manager()
+    out = mgr.dict()
+    mp.start_processes(_worker, args=(2, port, out), nprocs=2, start_method="spawn", join=True)
+    assert out[0] == out[1] == 55.5
+
+
+def test_whole_job_value():
+    # 2 replicas, 10 steps of 1 GB each, slowest rank 20 ms -> 1000 GB/s
+    assert bench.whole_job_gbs(10**9, 10, 2, 20.0) == pytest.approx(1000.0)
+    assert bench.max_over_ranks(3.0, 1, "cpu") == 3.0
+
+
+def test_byte_formulas_match_stated_sizes():
+    import oracle
+
+    g = group("llama70b")
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    assert bench.rs_bytes(g, lay.S, lay.U) == 8 * 855_654_400 * 2 + 8 * lay.S * 4
+    assert abs(bench.rs_bytes(g, lay.S, lay.U) / 1e9 - 17.113) < 0.001
+    assert bench.ag_bytes(lay.U) == 4 * 855_654_400
+
+
+def test_reference_arm_json_contract():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                          "--warmup", "3", "--workload", "llama8b"], capture_output=True, text=True, env=env,
+                         timeout=900)
+    assert res.returncode == 0, res.stderr
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0

@@ -1,0 +1,344 @@
+"""GPU parity of the CUDA path (called through the C ABI) against the CPU oracle.
+
+Reduced-size groups (the workload parameter lists with every dimension divided down, plus edge
+groups) are compared element by element, bit for bit, with 4 KiB canary guard bands around every
+device buffer and sentinel-prefilled outputs (so every output element must be written and every
+padding element must come out +0.0).  Full-size groups run in the launch configuration the
+benchmark times (default CTA counts) and are checked on sampled outputs that the oracle computes
+one by one from regenerated inputs, plus properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_pins
+from workloads import Group, group, rng
+
+pytestmark = pytest.mark.gpu
+
+GUARD_BYTES = 4096
+CANARY = 0x5A
+F32_SENTINEL = -1  # 0xFFFFFFFF, a NaN pattern no sum produces here
+BF16_SENTINEL = 0xBEEF - 65536
+BF16_JUNK = 0xDEAD - 65536
+
+
+@pytest.fixture(scope="module")
+def tide():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import all_gather_tide_gb300 as t
+
+    t.lib()
+    return t
+
+
+class Guarded:
+    """A device buffer with canary bytes before and after the payload view."""
+
+    def __init__(self, numel, dtype, fill=None, offset_elems=0, src=None):
+        es = torch.tensor([], dtype=dtype).element_size()
+        g = GUARD_BYTES // es
+        self.buf = torch.empty(2 * g + numel + offset_elems, dtype=dtype, device="cuda")
+        self.buf.view(torch.uint8).fill_(CANARY)
+        self.lo, self.hi = g + offset_elems, g + offset_elems + numel
+        self.view = self.buf[self.lo:self.hi]
+        if src is not None:
+            self.view.copy_(src)
+        elif fill is not None:
+            self.view.view(torch.int32 if es == 4 else torch.int16).fill_(fill)
+
+    def guards_intact(self) -> bool:
+        b = self.buf.view(torch.uint8)
+        es = self.buf.element_size()
+        head = b[: self.lo * es]
+        tail = b[self.hi * es:]
+        return bool((head == CANARY).all()) and bool((tail == CANARY).all())
+
+
+def f32_bits(t: torch.Tensor) -> np.ndarray:
+    return t.contiguous().view(torch.int32).cpu().numpy().view(np.uint32)
+
+
+def edge_groups():
+    return [
+        Group("single-rank", 1, (("a", 37, 5), ("b", 1024, 8), ("c", 3, 1))),
+        Group("one-row-64-ranks", 64, (("a", 1, 4096), ("b", 3, 8), ("c", 100, 1), ("d", 65, 3))),
+        Group("odd-offsets", 3, (("a", 7, 5), ("b", 1, 1), ("c", 11, 3), ("d", 300, 17))),
+        Group("ragged-tails", 8, (("a", 1001, 8), ("b", 13, 24), ("c", 40097, 1), ("d", 9, 4104))),
+        Group("integer-r16", 16, (("a", 333, 64), ("b", 64, 512), ("c", 17, 1)), grad_kind="int"),
+    ]
+
+
+def reduced_groups():
+    return [
+        group("tiny"),
+        group("llama8b").scaled(16),
+        group("qwen3moe").scaled(16),
+        group("llama70b").scaled(32),
+        group("wan_r8").scaled(8),
+        group("wan_r16").scaled(8),
+        group("wan_r32").scaled(16),
+        group("wan_r64").scaled(16),
+    ] + edge_groups()
+
+
+def _ids(gs):
+    return [g.name for g in gs]
+
+
+def run_rs(tide, g, ctas=0, misalign=False, flags=0):
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    host = rng.group_grads(g)
+    want = oracle.reduce_scatter(lay, [[t.numpy().view(np.uint16) for t in row] for row in host])
+    off = 1 if misalign else 0
+    grads = [[Guarded(t.numel(), torch.int16, src=t, offset_elems=off) for t in row] for row in host]
+    shards = [Guarded(lay.S, torch.float32, fill=F32_SENTINEL) for _ in range(g.R)]
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
+    G.set_ctas(ctas, 0)
+    G.reduce_scatter([[x.view for x in row] for row in grads], [s.view for s in shards])
+    torch.cuda.synchronize()
+    for d in range(g.R):
+        got = f32_bits(shards[d].view)
+        bad = np.nonzero(got != want[d].view(np.uint32))[0]
+        assert bad.size == 0, f"{g.name}: shard {d} differs at {bad[:8]} (of {bad.size})"
+        assert shards[d].guards_intact(), f"{g.name}: shard {d} guard band overwritten"
+    for row in grads:
+        for x in row:
+            assert x.guards_intact()
+    G.close()
+
+
+def run_ag(tide, g, ce=False, ctas=0, misalign=False, uniform=True, flags=0):
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    host = []
+    for r in range(g.R):
+        s = rng.shard_bits(g, r, lay.S).numpy().copy()
+        for p in range(g.P):  # junk in every padding position
+            v = lay.valid_rows(r, p) * int(lay.row_len[p])
+            s[int(lay.o[p]) + v: int(lay.o[p] + lay.s[p])] = BF16_JUNK
+        host.append(s)
+    want = oracle.all_gather(lay, [h.view(np.uint16) for h in host],
+                             [np.full(g.numel(p), BF16_SENTINEL & 0xFFFF, np.uint16) for p in range(g.P)])
+    off = 1 if misalign else 0
+    if uniform:
+        packed = Guarded(g.R * lay.S, torch.int16, src=torch.from_numpy(np.concatenate(host)), offset_elems=off)
+        shard_views = [packed.view[r * lay.S:(r + 1) * lay.S] for r in range(g.R)]
+        guards = [packed]
+    else:
+        guards = [Guarded(lay.S, torch.int16, src=torch.from_numpy(h), offset_elems=off) for h in host]
+        shard_views = [x.view for x in guards]
+    params = [Guarded(g.numel(p), torch.int16, fill=BF16_SENTINEL, offset_elems=off) for p in range(g.P)]
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
+    G.set_ctas(0, ctas)
+    if ce:
+        G.all_gather_ce(shard_views, [x.view for x in params])
+    else:
+        G.all_gather(shard_views, [x.view for x in params])
+    torch.cuda.synchronize()
+    for p in range(g.P):
+        got = params[p].view.cpu().numpy().view(np.uint16)
+        bad = np.nonzero(got != want[p])[0]
+        assert bad.size == 0, f"{g.name}: param {p} differs at {bad[:8]} (of {bad.size})"
+        assert not np.any(got == (BF16_JUNK & 0xFFFF))
+        assert params[p].guards_intact()
+    for x in guards:
+        assert x.guards_intact()
+    copies = G.last_ce_copies() if ce else None
+    G.close()
+    return copies
+
+
+# ---- reduced sizes, element by element -------------------------------------------------------
+
+
+@pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
+def test_reduce_scatter_matches_oracle(tide, g):
+    run_rs(tide, g)
+
+
+@pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
+def test_all_gather_matches_oracle(tide, g):
+    run_ag(tide, g)
+
+
+@pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
+def test_all_gather_ce_matches_oracle(tide, g):
+    copies, uniform = run_ag(tide, g, ce=True)
+    assert uniform
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    expect = sum((r // int(m) > 0) + (r % int(m) > 0) for r, m in zip(g.rows, lay.m))
+    assert copies == expect
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 17, 152, 1000])
+def test_cta_count_does_not_change_bits(tide, ctas):
+    run_rs(tide, group("qwen3moe").scaled(16), ctas=ctas)
+    run_ag(tide, group("qwen3moe").scaled(16), ctas=ctas)
+
+
+def test_misaligned_pointers_take_elementwise_path(tide):
+    g = group("llama8b").scaled(32)
+    run_rs(tide, g, misalign=True)
+    run_ag(tide, g, misalign=True)
+    run_ag(tide, g, misalign=True, ce=True)
+
+
+def test_vec_strict_rejects_misaligned(tide):
+    g = group("tiny")
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_VEC_STRICT)
+    grads = [[torch.zeros(g.numel(p) + 1, dtype=torch.bfloat16, device="cuda")[1:] for p in range(g.P)]
+             for _ in range(g.R)]
+    shards = [torch.zeros(G.S, dtype=torch.float32, device="cuda") for _ in range(g.R)]
+    with pytest.raises(tide.TideError) as e:
+        G.reduce_scatter(grads, shards)
+    assert e.value.status == tide.TIDE_EALIGN
+
+
+def test_ce_non_uniform_pitch_falls_back(tide):
+    g = group("qwen3moe").scaled(16)
+    copies, uniform = run_ag(tide, g, ce=True, uniform=False)
+    assert not uniform
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    assert copies == sum(1 for r in range(g.R) for p in range(g.P) if lay.valid_rows(r, p) > 0)
+
+
+def test_ce_strict_rejects_non_uniform_pitch(tide):
+    g = group("tiny")
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_CE_STRICT)
+    shards = [torch.zeros(G.S, dtype=torch.bfloat16, device="cuda") for _ in range(g.R)]
+    params = [torch.zeros(g.numel(p), dtype=torch.bfloat16, device="cuda") for p in range(g.P)]
+    with pytest.raises(tide.TideError) as e:
+        G.all_gather_ce(shards, params)
+    assert e.value.status == tide.TIDE_ELAYOUT
+
+
+def test_random_groups(tide):
+    for R, rows, row_len in oracle_pins.random_groups(21, 8):
+        g = Group(f"random-R{R}", R, tuple((f"p{i}", r, l) for i, (r, l) in enumerate(zip(rows, row_len))))
+        run_rs(tide, g)
+        run_ag(tide, g)
+        run_ag(tide, g, ce=True)
+
+
+def test_pointer_table_ring_and_streams(tide):
+    """Alternating buffer sets and streams reuse or refill the pointer-table ring correctly."""
+    g = group("llama70b").scaled(64)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+    sets = []
+    for k in range(6):
+        gg = Group(g.name, g.R, g.params, grad_seed_per_rank=False, grad_seed=100 + k)
+        host = rng.group_grads(gg)
+        want = oracle.reduce_scatter(lay, [[t.numpy().view(np.uint16) for t in row] for row in host])
+        dev = [[t.cuda() for t in row] for row in host]
+        out = [torch.empty(lay.S, dtype=torch.float32, device="cuda") for _ in range(g.R)]
+        sets.append((dev, out, want))
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    for it in range(3):
+        for k, (dev, out, want) in enumerate(sets):
+            st = streams[(k + it) % 2]
+            st.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(st):
+                for o in out:
+                    o.fill_(float("nan"))
+                G.reduce_scatter(dev, out)
+            torch.cuda.synchronize()
+            for d in range(g.R):
+                assert np.array_equal(f32_bits(out[d]), want[d].view(np.uint32)), (it, k, d)
+    G.close()
+
+
+# ---- full sizes, launch configuration of the benchmark ---------------------------------------
+
+FULL = ["llama8b", "qwen3moe", "llama70b", "wan_r8", "wan_r16", "wan_r32", "wan_r64"]
+
+
+def _sample_positions(lay, seed, n=3000):
+    """Random shard positions plus the first/last element of every piece and both sides of
+    every valid/padding boundary."""
+    rs = np.random.default_rng(seed)
+    d = list(rs.integers(0, lay.R, n))
+    j = list(rs.integers(0, lay.S, n))
+    for dd in range(lay.R):
+        for p in range(lay.P):
+            o, s = int(lay.o[p]), int(lay.s[p])
+            v = lay.valid_rows(dd, p) * int(lay.row_len[p])
+            for x in {o, o + s - 1, o + v - 1, o + v}:
+                if o <= x < o + s:
+                    d.append(dd)
+                    j.append(x)
+    return np.asarray(d, np.int64), np.asarray(j, np.int64)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_reduce_scatter(tide, name):
+    g = group(name)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    grads = [[rng.grad_bits(g, r, p, device="cuda").view(torch.bfloat16) for p in range(g.P)] for r in range(g.R)]
+    shards = torch.empty(g.R, lay.S, dtype=torch.float32, device="cuda")
+    shards.view(torch.int32).fill_(F32_SENTINEL)
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+    G.reduce_scatter(grads, list(shards))
+    torch.cuda.synchronize()
+    # (1) sampled outputs, computed one by one by the oracle from regenerated inputs
+    d, j = _sample_positions(lay, seed=len(name))
+    want = oracle.rs_points(lay, d, j, lambda r, p, idx: rng.grad_bits(g, r, p, idx=torch.from_numpy(idx))
+                            .numpy().view(np.uint16))
+    got = shards[torch.from_numpy(d).cuda(), torch.from_numpy(j).cuda()]
+    assert np.array_equal(f32_bits(got), want.view(np.uint32))
+    # (2) every element written; every padding element +0.0; every piece equal to torch fp32 adds in
+    # ascending rank order (the definition, evaluated with torch on the device)
+    assert not bool((shards.view(torch.int32) == F32_SENTINEL).any())
+    for dd in range(g.R):
+        for p in range(g.P):
+            o, s, L = int(lay.o[p]), int(lay.s[p]), int(lay.row_len[p])
+            v = lay.valid_rows(dd, p) * L
+            piece = shards[dd, o:o + s]
+            assert bool((piece[v:].view(torch.int32) == 0).all())
+            if v:
+                acc = grads[0][p][dd * s: dd * s + v].float()
+                for r in range(1, g.R):
+                    acc = acc + grads[r][p][dd * s: dd * s + v].float()
+                assert torch.equal(piece[:v].view(torch.int32), acc.view(torch.int32)), (dd, p)
+    # (3) total over all shards = total gradient (fp64), within the fp32 fold bound
+    tot_in = sum(grads[r][p].double().sum() for r in range(g.R) for p in range(g.P)).item()
+    abs_in = sum(grads[r][p].double().abs().sum() for r in range(g.R) for p in range(g.P)).item()
+    tot_out = shards.double().sum().item()
+    assert abs(tot_out - tot_in) <= (g.R - 1) * 2.0 ** -24 * abs_in
+    G.close()
+    del grads, shards
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_all_gather(tide, name):
+    g = group(name)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    shards = torch.stack([rng.shard_bits(g, r, lay.S, device="cuda") for r in range(g.R)])
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+    for ce in (False, True):
+        params = [torch.full((g.numel(p),), BF16_SENTINEL, dtype=torch.int16, device="cuda") for p in range(g.P)]
+        (G.all_gather_ce if ce else G.all_gather)(list(shards), params)
+        torch.cuda.synchronize()
+        rs = np.random.default_rng(7)
+        for p in range(g.P):
+            n = g.numel(p)
+            idx = np.unique(np.concatenate([rs.integers(0, n, 64), [0, n - 1]]))
+            r, jj = oracle.ag_points(lay, p, idx)
+            want = np.zeros(idx.size, np.int64)
+            for a in np.unique(r):
+                sel = r == a
+                want[sel] = rng.shard_bits(g, int(a), 0, idx=torch.from_numpy(jj[sel])).numpy().astype(np.int64)
+            want &= 0xFFFF
+            got = params[p][torch.from_numpy(idx).cuda()].cpu().numpy().astype(np.int64) & 0xFFFF
+            assert np.array_equal(got, want), (ce, p)
+            for rr in range(g.R):
+                v = lay.valid_rows(rr, p) * int(lay.row_len[p])
+                s, o = int(lay.s[p]), int(lay.o[p])
+                assert torch.equal(params[p][rr * s: rr * s + v], shards[rr, o:o + v]), (ce, p, rr)
+        del params
+    G.close()
+    del shards
+    torch.cuda.empty_cache()

@@ -84,3 +84,11 @@ def test_wan_sweep_fill_rule(R, P):
     assert [(r, l) for _, r, l in g.params[:-1]] == [(r, l) for _, r, l in ps]
     assert g.params[-1][1:] == (R * rem, 1)
     assert any(r % R for r in g.rows)
+
+
+def test_positions_match_ranges():
+    idx = torch.tensor([0, 5, 1234, 77, 2999])
+    full = rng.normal_bf16_bits(2, 3, 4, 3000, 1e-3)
+    assert torch.equal(rng.normal_bf16_bits(2, 3, 4, 0, 1e-3, idx=idx), full[idx])
+    fi = rng.uniform_int_bf16_bits(2, 3, 4, 3000)
+    assert torch.equal(rng.uniform_int_bf16_bits(2, 3, 4, 0, idx=idx), fi[idx])

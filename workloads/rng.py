@@ -79,18 +79,24 @@ def _f32_to_bf16_bits(x: torch.Tensor) -> torch.Tensor:
     return b.to(torch.int16)
 
 
-def _fill(out: torch.Tensor, start: int, fn) -> torch.Tensor:
-    numel = out.numel()
-    for a in range(0, numel, _CHUNK):
-        b = min(numel, a + _CHUNK)
+def _fill(numel: int, start: int, idx, device, fn) -> torch.Tensor:
+    """Elements ``start .. start+numel-1`` of a stream, or the elements at positions ``idx``."""
+    if idx is not None:
+        idx = torch.as_tensor(idx, dtype=torch.int64).to(device)
+        return fn(idx.reshape(-1)).reshape(idx.shape)
+    out = torch.empty(numel, dtype=torch.int16, device=device)
+    step = _CHUNK * (4 if out.is_cuda else 1)
+    for a in range(0, numel, step):
+        b = min(numel, a + step)
         i = torch.arange(start + a, start + b, dtype=torch.int64, device=out.device)
         out[a:b] = fn(i)
     return out
 
 
 def uniform_int_bf16_bits(seed: int, rank: int, stream: int, numel: int, lo: int = -8, hi: int = 8,
-                          device="cpu", start: int = 0) -> torch.Tensor:
-    """Integers uniform on ``[lo, hi]`` (inclusive), as bf16 bits; elements ``start .. start+numel-1``."""
+                          device="cpu", start: int = 0, idx=None) -> torch.Tensor:
+    """Integers uniform on ``[lo, hi]`` (inclusive), as bf16 bits; elements ``start .. start+numel-1``
+    (or the positions in ``idx``)."""
     key = stream_key(seed, rank, stream)
     span = hi - lo + 1
 
@@ -98,11 +104,11 @@ def uniform_int_bf16_bits(seed: int, rank: int, stream: int, numel: int, lo: int
         v = (_lsr(_draw(key, i), 32) % span + lo).to(torch.float32)
         return _f32_to_bf16_bits(v)
 
-    return _fill(torch.empty(numel, dtype=torch.int16, device=device), start, fn)
+    return _fill(numel, start, idx, device, fn)
 
 
 def normal_bf16_bits(seed: int, rank: int, stream: int, numel: int, sigma: float,
-                     device="cpu", start: int = 0) -> torch.Tensor:
+                     device="cpu", start: int = 0, idx=None) -> torch.Tensor:
     """N(0, sigma) stand-in (Irwin-Hall of twelve 16-bit uniforms) as bf16 bits."""
     key = stream_key(seed, rank, stream)
     scale = float(torch.tensor(sigma / 65536.0, dtype=torch.float32))
@@ -115,15 +121,17 @@ def normal_bf16_bits(seed: int, rank: int, stream: int, numel: int, sigma: float
         z = (k - 393210).to(torch.float32)  # 12 * 65535 / 2 = 393210; |z| < 2**19, exact
         return _f32_to_bf16_bits(z * scale)
 
-    return _fill(torch.empty(numel, dtype=torch.int16, device=device), start, fn)
+    return _fill(numel, start, idx, device, fn)
 
 
-def grad_bits(g, r: int, p: int, device="cpu", start: int = 0, numel: Optional[int] = None) -> torch.Tensor:
-    """Gradient of parameter ``p`` on rank ``r`` of group ``g`` (flat, row-major), as bf16 bits."""
+def grad_bits(g, r: int, p: int, device="cpu", start: int = 0, numel: Optional[int] = None,
+              idx=None) -> torch.Tensor:
+    """Gradient of parameter ``p`` on rank ``r`` of group ``g`` (flat, row-major), as bf16 bits
+    (the whole tensor, a range from ``start``, or the positions ``idx``)."""
     n = g.numel(p) - start if numel is None else numel
     if g.grad_kind == "int":
-        return uniform_int_bf16_bits(g.grad_seed_of(r), r, p, n, -8, 8, device=device, start=start)
-    return normal_bf16_bits(g.grad_seed_of(r), r, p, n, g.grad_sigma, device=device, start=start)
+        return uniform_int_bf16_bits(g.grad_seed_of(r), r, p, n, -8, 8, device=device, start=start, idx=idx)
+    return normal_bf16_bits(g.grad_seed_of(r), r, p, n, g.grad_sigma, device=device, start=start, idx=idx)
 
 
 def group_grads(g, device="cpu") -> List[List[torch.Tensor]]:
@@ -131,10 +139,10 @@ def group_grads(g, device="cpu") -> List[List[torch.Tensor]]:
     return [[grad_bits(g, r, p, device) for p in range(g.P)] for r in range(g.R)]
 
 
-def shard_bits(g, r: int, numel: int, device="cpu", start: int = 0) -> torch.Tensor:
+def shard_bits(g, r: int, numel: int, device="cpu", start: int = 0, idx=None) -> torch.Tensor:
     """Packed all-gather input shard of rank ``r`` (``numel`` elements), N(0, shard_sigma) bits.
 
     Every element is drawn, padding positions included; a caller that wants a recognisable junk
     pattern in the padding overwrites those positions itself."""
     return normal_bf16_bits(g.shard_seed_of(r), r, SHARD_STREAM, numel, g.shard_sigma,
-                            device=device, start=start)
+                            device=device, start=start, idx=idx)
