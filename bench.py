@@ -372,9 +372,9 @@ def interference(G, buf, stream, dev, args):
                     "tflops": 2 * M * N * K / (t_alone * 1e-3) / 1e12, "library": "cuBLAS via torch.matmul"}}
     rs_default, ag_default = G.get_ctas()
     out["reduce_scatter"] = dict(ctas=rs_default, **concurrent(lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream), "rs"))
-    for c in args.interference_ctas:
-        G.set_ctas(c, 0)
-        out[f"reduce_scatter_ctas{c}"] = dict(ctas=c, **concurrent(
+    for n_ctas in args.interference_ctas:
+        G.set_ctas(n_ctas, 0)
+        out[f"reduce_scatter_ctas{n_ctas}"] = dict(ctas=n_ctas, **concurrent(
             lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream), "rs"))
     G.set_ctas(args.rs_ctas, args.ag_ctas)
     # the placement is short; run it several times back to back so GEMMs fit inside

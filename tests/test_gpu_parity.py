@@ -127,8 +127,13 @@ def run_ag(tide, g, ce=False, ctas=0, misalign=False, uniform=True, flags=0):
         shard_views = [packed.view[r * lay.S:(r + 1) * lay.S] for r in range(g.R)]
         guards = [packed]
     else:
-        guards = [Guarded(lay.S, torch.int16, src=torch.from_numpy(h), offset_elems=off) for h in host]
-        shard_views = [x.view for x in guards]
+        # one buffer, shards separated by growing gaps: no single pitch fits
+        starts = [r * lay.S + 8 * r * (r + 1) // 2 for r in range(g.R)]
+        packed = Guarded(starts[-1] + lay.S, torch.int16, fill=0, offset_elems=off)
+        shard_views = [packed.view[a:a + lay.S] for a in starts]
+        for v, h in zip(shard_views, host):
+            v.copy_(torch.from_numpy(h))
+        guards = [packed]
     params = [Guarded(g.numel(p), torch.int16, fill=BF16_SENTINEL, offset_elems=off) for p in range(g.P)]
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
     G.set_ctas(0, ctas)
@@ -207,7 +212,8 @@ def test_ce_non_uniform_pitch_falls_back(tide):
 def test_ce_strict_rejects_non_uniform_pitch(tide):
     g = group("tiny")
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_CE_STRICT)
-    shards = [torch.zeros(G.S, dtype=torch.bfloat16, device="cuda") for _ in range(g.R)]
+    buf = torch.zeros(16 * G.S, dtype=torch.bfloat16, device="cuda")
+    shards = [buf[a:a + G.S] for a in (0, 2 * G.S, 3 * G.S, 6 * G.S)]  # pitches 2S, S, 3S
     params = [torch.zeros(g.numel(p), dtype=torch.bfloat16, device="cuda") for p in range(g.P)]
     with pytest.raises(tide.TideError) as e:
         G.all_gather_ce(shards, params)
