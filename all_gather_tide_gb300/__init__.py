@@ -50,6 +50,7 @@ SIGNATURES = {
     "tide_all_gather": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_all_gather_ce": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_group_last_ce_copies": (ctypes.c_int, [_vp, _i64p, _i32p]),
+    "tide_reduce_scatter_noalloc": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _vpp, _vpp, _vp]),
     "tide_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "tide_last_cuda_error": (ctypes.c_int, []),
     "tide_version": (ctypes.c_int, []),
@@ -200,6 +201,16 @@ def tide_all_gather(g: int, shards: Sequence, params: Sequence, stream=None) -> 
 def tide_all_gather_ce(g: int, shards: Sequence, params: Sequence, stream=None) -> None:
     _check(lib().tide_all_gather_ce(g, _ptr_array(shards), _ptr_array(params), _stream(stream)),
            "tide_all_gather_ce")
+
+
+def tide_reduce_scatter_noalloc(R: int, rows: Sequence[int], row_len: Sequence[int], grads, shards: Sequence,
+                                stream=None) -> None:
+    """Reduce-scatter without any allocation (for callers that cannot allocate device memory):
+    the work tables go to the library's fixed device scratch array.  Same data layout as
+    ``tide_reduce_scatter``; calls on different streams must not overlap."""
+    _check(lib().tide_reduce_scatter_noalloc(R, len(rows), _i64_array(rows), _i64_array(row_len),
+                                             _ptr_array(_flat_grads(grads)), _ptr_array(shards), _stream(stream)),
+           "tide_reduce_scatter_noalloc")
 
 
 def tide_group_last_ce_copies(g: int) -> Tuple[int, bool]:

@@ -42,6 +42,8 @@ struct Slot {
 
 }  // namespace
 
+int tide::record_cuda_error(cudaError_t e) { return cuda_fail(e); }
+
 struct tide_group {
     tide::Plan plan;
     uint32_t flags = 0;

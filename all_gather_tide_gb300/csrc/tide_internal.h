@@ -62,6 +62,9 @@ int make_layout(int32_t R, int32_t P, const int64_t* rows, const int64_t* row_le
 void make_work_lists(Plan* plan);
 int64_t valid_rows(int64_t rows_p, int64_t m_p, int64_t d);
 
+// Stores `e` as this host thread's last CUDA error (tide_last_cuda_error) and returns TIDE_ECUDA.
+int record_cuda_error(cudaError_t e);
+
 // Kernel launchers (stream-ordered; return the launch status).
 cudaError_t launch_reduce_scatter(const RsSeg* segs, int nsegs, int64_t nchunks,
                                   const uint16_t* const* grads, float* const* shards, int R, int P,

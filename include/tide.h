@@ -148,6 +148,37 @@ int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *p
 /* Copies issued by the last tide_all_gather_ce on g, and whether the uniform-pitch form was used. */
 int tide_group_last_ce_copies(tide_group_t g, int64_t *copies, int32_t *uniform_pitch);
 
+/* ---- reduce-scatter without allocation ---------------------------------------------------- */
+/* Size of the library's fixed device scratch array used by tide_reduce_scatter_noalloc. */
+#define TIDE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/*
+ * tide_reduce_scatter_noalloc — the same reduce-scatter as tide_reduce_scatter, for callers that
+ * must not allocate memory.  The paper has no counterpart: it is a deployment variant of this
+ * library.  tide_group_create allocates device tables and pinned host slots; a caller whose
+ * framework has already reserved nearly all device memory in its own caching allocator, or that
+ * cannot afford cudaMalloc/cudaFree (they may synchronise the device) while communication runs
+ * beside compute, can call this instead.  It takes the group description and the pointers
+ * directly (same meaning and layout as tide_group_create + tide_reduce_scatter), plans the group
+ * on the host at every call, copies the work tables into a fixed device array of
+ * TIDE_NOALLOC_SCRATCH_BYTES that the library carries (every GPU that loads the library holds it
+ * until the process exits), and launches the reduce-scatter kernel with the default CTA count.
+ * It calls no cudaMalloc, cudaFree or other allocating CUDA routine.
+ *   - Size limit: the tables take round_up(56*R*P, 256) + 8*(R*P + R) bytes; a group whose
+ *     tables do not fit in TIDE_NOALLOC_SCRATCH_BYTES is rejected with TIDE_ERANGE before
+ *     anything is enqueued.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's tables; nothing in it has to
+ *     start at zero, because each call rewrites everything its kernel reads.  Calls on the same
+ *     stream are ordered; calls that overlap on the GPU (different streams, or several host
+ *     threads on different streams) race on the array and must not be issued.
+ * Errors: as tide_plan_layout and tide_reduce_scatter (no TIDE_FLAG_VEC_STRICT: unaligned pointers
+ * take the element-wise path), TIDE_ERANGE as above, TIDE_ECUDA.
+ */
+int tide_reduce_scatter_noalloc(int32_t R, int32_t P, const int64_t *rows, const int64_t *row_len,
+                                const void *const *grads, void *const *shards, void *stream);
+
 /* ---- errors ------------------------------------------------------------------------------ */
 const char *tide_strerror(int status);
 /* cudaError_t code of the last CUDA failure reported as TIDE_ECUDA on this host thread. */
