@@ -336,6 +336,8 @@ def interference(G, buf, stream, dev, args):
     t_alone = statistics.median(alone)
 
     def concurrent(launch, label, reps=4):
+        """GEMMs back to back on the second stream from the collective's start; a GEMM counts if it
+        starts while the collective runs, and its time includes any wait for free SMs."""
         inside = []
         coll_ms = []
         for _ in range(reps):
@@ -357,10 +359,9 @@ def interference(G, buf, stream, dev, args):
             end = s0.elapsed_time(s1)
             coll_ms.append(end)
             for e in ge:
-                st, en = s0.elapsed_time(e[0]), s0.elapsed_time(e[1])
-                if st >= 0 and en <= end:
+                if 0 <= s0.elapsed_time(e[0]) < end:
                     inside.append(e[0].elapsed_time(e[1]))
-        res = {"collective_ms": statistics.median(coll_ms), "gemms_inside": len(inside)}
+        res = {"collective_ms": statistics.median(coll_ms), "gemms_started_inside": len(inside)}
         if inside:
             res["gemm_ms"] = statistics.median(inside)
             res["slowdown_pct"] = 100.0 * (statistics.median(inside) / t_alone - 1.0)
@@ -370,6 +371,8 @@ def interference(G, buf, stream, dev, args):
 
     out = {"gemm": {"M": M, "N": N, "K": K, "dtype": "bf16", "alone_ms": t_alone,
                     "tflops": 2 * M * N * K / (t_alone * 1e-3) / 1e12, "library": "cuBLAS via torch.matmul"}}
+    if args.sweep:
+        out["cta_sweep"] = cta_sweep(G, buf, stream, args, concurrent)
     rs_default, ag_default = G.get_ctas()
     out["reduce_scatter"] = dict(ctas=rs_default, **concurrent(lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream), "rs"))
     for n_ctas in args.interference_ctas:
@@ -383,6 +386,41 @@ def interference(G, buf, stream, dev, args):
     out["all_gather_ce"] = dict(ctas=0, **concurrent(
         lambda: [G.all_gather_ce(buf.ag_list, buf.params, stream) for _ in range(8)], "ce"))
     return out
+
+
+def cta_sweep(G, buf, stream, args, concurrent):
+    """Collective bandwidth alone and concurrent-GEMM slowdown per CTA count (the Pareto curve
+    between collective speed and interference; Fig. 4 and Table 4 of the paper)."""
+    g_rs = rs_bytes_of(G)
+    g_ag = 4 * G.U
+    rows = []
+    for kind, counts in (("reduce_scatter", args.sweep_rs), ("all_gather_sm", args.sweep_ag)):
+        for n in counts:
+            if kind == "reduce_scatter":
+                G.set_ctas(n, 0)
+                launch = lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream)
+                nbytes, reps = g_rs, 1
+            else:
+                G.set_ctas(0, n)
+                launch = lambda: [G.all_gather(buf.ag_list, buf.params, stream) for _ in range(8)]
+                nbytes, reps = g_ag * 8, 8
+            with torch.cuda.stream(stream):
+                launch()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                launch()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            c = concurrent(launch, kind, reps=2)
+            rows.append({"kind": kind, "ctas": n, "alone_ms": ms / reps, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                         "gemm_slowdown_pct": c["slowdown_pct"], "gemms": c["gemms_started_inside"]})
+    G.set_ctas(args.rs_ctas, args.ag_ctas)
+    return rows
+
+
+def rs_bytes_of(G) -> int:
+    return G.R * G.U * 2 + G.R * G.S * 4
 
 
 # ---- end to end with host buffers --------------------------------------------------------------
@@ -522,6 +560,9 @@ def main():
     ap.add_argument("--interference-ctas", type=int, nargs="*", default=[16, 32])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-reps", type=int, default=4)
+    ap.add_argument("--sweep", action="store_true", help="CTA-count sweep of bandwidth vs GEMM slowdown")
+    ap.add_argument("--sweep-rs", type=int, nargs="*", default=[8, 16, 20, 24, 32, 48, 64, 96, 152, 304])
+    ap.add_argument("--sweep-ag", type=int, nargs="*", default=[8, 16, 24, 32, 64, 152, 608])
     ap.add_argument("--no-interference", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
