@@ -28,6 +28,10 @@ TIDE_ENOMEM = -5
 TIDE_ERANGE = -6
 TIDE_FLAG_VEC_STRICT = 0x1
 TIDE_FLAG_CE_STRICT = 0x2
+TIDE_RS_AUTO = 0
+TIDE_RS_REGISTER = 1
+TIDE_RS_BULK = 2
+TIDE_DEBUG_STALL_PRODUCER = 0x1
 
 _lib = None
 _i64p = ctypes.POINTER(ctypes.c_int64)
@@ -50,6 +54,10 @@ SIGNATURES = {
     "tide_all_gather": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_all_gather_ce": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_group_last_ce_copies": (ctypes.c_int, [_vp, _i64p, _i32p]),
+    "tide_group_set_rs_variant": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "tide_group_set_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_uint64]),
+    "tide_group_device_status": (ctypes.c_int, [_vp, _i32p]),
+    "tide_group_set_debug": (ctypes.c_int, [_vp, ctypes.c_uint32]),
     "tide_reduce_scatter_noalloc": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _vpp, _vpp, _vp]),
     "tide_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "tide_last_cuda_error": (ctypes.c_int, []),
@@ -203,6 +211,24 @@ def tide_all_gather_ce(g: int, shards: Sequence, params: Sequence, stream=None) 
            "tide_all_gather_ce")
 
 
+def tide_group_set_rs_variant(g: int, variant: int) -> None:
+    _check(lib().tide_group_set_rs_variant(g, variant), "tide_group_set_rs_variant")
+
+
+def tide_group_set_wait_timeout(g: int, timeout_ns: int) -> None:
+    _check(lib().tide_group_set_wait_timeout(g, timeout_ns), "tide_group_set_wait_timeout")
+
+
+def tide_group_device_status(g: int) -> int:
+    v = ctypes.c_int32()
+    _check(lib().tide_group_device_status(g, ctypes.byref(v)), "tide_group_device_status")
+    return v.value
+
+
+def tide_group_set_debug(g: int, flags: int) -> None:
+    _check(lib().tide_group_set_debug(g, flags), "tide_group_set_debug")
+
+
 def tide_reduce_scatter_noalloc(R: int, rows: Sequence[int], row_len: Sequence[int], grads, shards: Sequence,
                                 stream=None) -> None:
     """Reduce-scatter without any allocation (for callers that cannot allocate device memory):
@@ -274,3 +300,15 @@ class Group:
 
     def last_ce_copies(self) -> Tuple[int, bool]:
         return tide_group_last_ce_copies(self.handle)
+
+    def set_rs_variant(self, variant: int) -> None:
+        tide_group_set_rs_variant(self.handle, variant)
+
+    def set_wait_timeout(self, timeout_ns: int) -> None:
+        tide_group_set_wait_timeout(self.handle, timeout_ns)
+
+    def device_status(self) -> int:
+        return tide_group_device_status(self.handle)
+
+    def set_debug(self, flags: int) -> None:
+        tide_group_set_debug(self.handle, flags)

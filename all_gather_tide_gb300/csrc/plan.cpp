@@ -75,6 +75,16 @@ void make_work_lists(Plan* pl) {
     }
     pl->rs_chunks = chunks;
 
+    // The same pieces cut into the bulk-copy kernel's larger chunks.
+    pl->rs_bulk.clear();
+    chunks = 0;
+    for (RsSeg sg : pl->rs) {
+        sg.chunk_begin = chunks;
+        chunks += (sg.total + kBulkChunk - 1) / kBulkChunk;
+        pl->rs_bulk.push_back(sg);
+    }
+    pl->rs_bulk_chunks = chunks;
+
     // All-gather placement: source-rank-major runs of valid elements; padding never appears.
     pl->ag.clear();
     chunks = 0;

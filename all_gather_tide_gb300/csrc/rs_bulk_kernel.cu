@@ -1,0 +1,383 @@
+// Reduce-scatter kernel with bulk asynchronous copies into shared memory (sm_103a).
+//
+// Paper: "The Endgame of FSDP Communication" (arXiv 2610.38228).  Fig. 2b step 5 and Fig. 6a form
+// the fp32 sums in a bounded number of short-lived CTAs fed by bulk (TMA) copies, so that few SMs
+// are taken from concurrent compute (Fig. 3, Fig. 4, Table 4).  With few CTAs the register-path
+// kernel is limited by the bytes one SM keeps in flight; this variant keeps a deep pipeline of
+// bulk copies in flight per SM instead.
+//
+// The bulk-copy engine of an SM keeps only a few copies in flight, so its bandwidth grows with the
+// size of each copy (measured on GB300: about 17 GB/s per SM with 4 KB copies, about 185 GB/s per
+// SM with 48 KB copies).  The kernel therefore streams one rank's row of a chunk per copy: a chunk
+// is kBulkChunk elements of one (destination, parameter) piece, and its R rows pass through
+// kBulkStages shared-memory stages of kBulkChunk bf16 elements, rank 0 first.  The fp32 sums of
+// the chunk stay in the consumers' registers across the R stages (ascending rank order, starting
+// from rank 0's value, exact bf16 -> fp32 widening, __fadd_rn), and are stored once, straight to
+// the destination shard (st.global.cs), after the last rank.
+//
+// One CTA = 1 producer warp (lane 0 issues the copies) + kBulkConsumerWarps consumer warps; one
+// CTA per SM.  Per stage the producer waits on the stage's `empty` mbarrier, announces the byte
+// count on its `full` mbarrier and issues one cp.async.bulk; consumers wait on `full`, add their
+// slice of the row with mixed-precision adds (add.rn.f32.bf16: the bf16 operand widened exactly,
+// the fp32 sum rounded to nearest even; one instruction per element), and release the stage.  Elements a bulk copy cannot carry (a piece whose
+// offsets are not 16-byte compatible, the < 8-element tail of the valid rows) are read with plain
+// loads, and padding is stored as zeros, exactly as in the register-path kernel: the results are
+// the same bits.
+//
+// Every mbarrier wait is bounded by %globaltimer: after `timeout_ns` the waiting thread records
+// an error code in *status, all warps stop, the producer waits (again bounded) for the copies it
+// has in flight, and the CTA returns.  Nothing traps.
+#include <algorithm>
+
+#include "tide_internal.h"
+
+namespace tide {
+namespace {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.  Both addresses 16-byte
+// aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// acc0 = fp32(low bf16 of w), acc1 = fp32(high bf16 of w): exact widening.
+__device__ __forceinline__ void first_pair(float& acc0, float& acc1, uint32_t w) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.f32.bf16 %0, l;\n\tcvt.f32.bf16 %1, h;\n\t}"
+        : "=f"(acc0), "=f"(acc1)
+        : "r"(w));
+}
+
+// acc0 += low bf16 of w, acc1 += high bf16 of w: mixed-precision adds (the bf16 operand is widened
+// exactly, the fp32 sum is rounded to nearest even; no flush to zero).
+__device__ __forceinline__ void add_pair(float& acc0, float& acc1, uint32_t w) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\tadd.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(acc0), "+f"(acc1)
+        : "r"(w));
+}
+
+// Adds (First: widens) this thread's groups of one rank row held in shared memory.
+template <bool First, int Groups, int Consumers>
+__device__ __forceinline__ void accumulate_row(float (&acc)[Groups][8], const uint4* row, int ctid, bool whole,
+                                               int64_t nbulk) {
+#pragma unroll
+    for (int j = 0; j < Groups; ++j) {
+        const int g = j * Consumers + ctid;  // 8-element group index in the chunk
+        if (whole || int64_t(g) * 8 + 8 <= nbulk) {
+            const uint4 w = row[g];
+            if (First) {
+                first_pair(acc[j][0], acc[j][1], w.x);
+                first_pair(acc[j][2], acc[j][3], w.y);
+                first_pair(acc[j][4], acc[j][5], w.z);
+                first_pair(acc[j][6], acc[j][7], w.w);
+            } else {
+                add_pair(acc[j][0], acc[j][1], w.x);
+                add_pair(acc[j][2], acc[j][3], w.y);
+                add_pair(acc[j][4], acc[j][5], w.z);
+                add_pair(acc[j][6], acc[j][7], w.w);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ uint16_t ld_u16(const uint16_t* p) {
+    unsigned short v;
+    asm("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float bf16_f32(uint16_t b) { return __uint_as_float(uint32_t(b) << 16); }
+
+__device__ __forceinline__ float sum_scalar(const uint16_t* const* __restrict__ grads, int R, int P, int p,
+                                            int64_t idx) {
+    float acc = bf16_f32(ld_u16(grads[p] + idx));
+    for (int r = 1; r < R; ++r) acc = __fadd_rn(acc, bf16_f32(ld_u16(grads[int64_t(r) * P + p] + idx)));
+    return acc;
+}
+
+__device__ __forceinline__ int find_piece(const RsSeg* __restrict__ segs, int nsegs, int cur, int64_t c) {
+    if (cur + 1 >= nsegs || segs[cur + 1].chunk_begin > c) return cur;
+    int lo = cur + 1, hi = nsegs, step = 1;
+    for (;;) {
+        const int nxt = lo + step;
+        if (nxt >= nsegs) break;
+        if (segs[nxt].chunk_begin > c) {
+            hi = nxt;
+            break;
+        }
+        lo = nxt;
+        step <<= 1;
+    }
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (segs[mid].chunk_begin <= c) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// Chunk geometry shared by producer and consumers.
+struct ChunkView {
+    int64_t n;       // elements in the chunk
+    int64_t nvalid;  // of which are sums
+    int64_t nbulk;   // leading valid elements delivered by bulk copies (multiple of 8, 0 if none)
+    int64_t src;     // element offset of the chunk in every rank's gradient of p
+    int64_t dst;     // element offset of the chunk in shard d
+    int d, p;
+};
+
+__device__ __forceinline__ ChunkView view_of(const RsSeg& sg, int64_t c, int64_t chunk, int allow_vec) {
+    ChunkView v;
+    const int64_t base = (c - sg.chunk_begin) * chunk;
+    v.n = min(chunk, sg.total - base);
+    v.nvalid = max(int64_t(0), min(v.n, sg.valid - base));
+    v.nbulk = (allow_vec && sg.vec) ? (v.nvalid & ~int64_t(7)) : 0;
+    v.src = sg.src_off + base;
+    v.dst = sg.dst_off + base;
+    v.d = sg.d;
+    v.p = sg.p;
+    return v;
+}
+
+constexpr uint64_t kTimerCheckEvery = 256;
+
+// Wait for the phase of `bar` with the given parity, for at most `timeout_ns` from the first
+// failed try.  Returns false (after recording `code` in *status and raising the CTA's abort flag)
+// when the time runs out, or when another warp of the CTA has aborted.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns,
+                                             volatile int* abort, int* status, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t deadline = globaltimer() + timeout_ns;
+    uint64_t spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if (++spins % kTimerCheckEvery == 0) {
+            if (*abort) return false;
+            if (globaltimer() > deadline) {
+                atomicCAS(status, 0, code);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+// The piece holding the current chunk, cached across the chunks of one piece (chunks only move
+// forward), so a chunk normally costs no table load at all.
+struct PieceCursor {
+    int cur = -1;
+    int64_t next_begin = 0;  // first chunk of the next piece
+    int64_t dst_off = 0, src_off = 0, valid = 0, total = 0, chunk_begin = 0;
+    int d = 0, p = 0, vec = 0;
+
+    // Moves to the piece holding chunk c; true when it changed.
+    __device__ __forceinline__ bool seek(const RsSeg* __restrict__ segs, int nsegs, int64_t c) {
+        if (cur >= 0 && c < next_begin) return false;
+        cur = find_piece(segs, nsegs, cur < 0 ? 0 : cur, c);
+        const RsSeg* q = segs + cur;
+        dst_off = __ldg(&q->dst_off);
+        src_off = __ldg(&q->src_off);
+        valid = __ldg(&q->valid);
+        total = __ldg(&q->total);
+        chunk_begin = __ldg(&q->chunk_begin);
+        d = __ldg(&q->d);
+        p = __ldg(&q->p);
+        vec = __ldg(&q->vec);
+        next_begin = cur + 1 < nsegs ? __ldg(&segs[cur + 1].chunk_begin) : INT64_MAX;
+        return true;
+    }
+
+    __device__ __forceinline__ ChunkView view(int64_t c, int64_t chunk, int allow_vec) const {
+        ChunkView v;
+        const int64_t base = (c - chunk_begin) * chunk;
+        v.n = min(chunk, total - base);
+        v.nvalid = max(int64_t(0), min(v.n, valid - base));
+        v.nbulk = (allow_vec && vec) ? (v.nvalid & ~int64_t(7)) : 0;
+        v.src = src_off + base;
+        v.dst = dst_off + base;
+        v.d = d;
+        v.p = p;
+        return v;
+    }
+};
+
+__device__ __forceinline__ void st_cs_v8(float* p, const float (&a)[8]) {
+    asm volatile("st.global.cs.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a[0]), "f"(a[1]),
+                 "f"(a[2]), "f"(a[3]), "f"(a[4]), "f"(a[5]), "f"(a[6]), "f"(a[7])
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(kBulkThreads, 1)
+reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nchunks,
+                           const uint16_t* const* __restrict__ grads, float* const* __restrict__ shards, int R,
+                           int P, int allow_vec, int* status, uint64_t timeout_ns, int inject) {
+    constexpr int kConsumers = kBulkConsumerWarps * 32;
+    constexpr int kGroups = int(kBulkChunk / 8 / kConsumers);  // 8-element groups per consumer thread
+    static_assert(kBulkChunk % (8 * kConsumers) == 0, "chunk must split evenly over the consumers");
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kBulkStages;
+    unsigned char* data = smem + 128;  // stage s at data + s * kBulkChunk * 2
+    // the R gradient pointers of the producer's current piece
+    const uint16_t** gptr = reinterpret_cast<const uint16_t**>(data + int64_t(kBulkStages) * kBulkChunk * 2);
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kBulkStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kBulkConsumerWarps);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    volatile int* abort = &abort_flag;
+
+    if (warp == kBulkConsumerWarps) {
+        // ---------------- producer warp: all lanes track the piece, lane 0 issues ----------------
+        PieceCursor pc;
+        int64_t it = 0;  // stage uses issued so far (lane 0)
+        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+            if (pc.seek(segs, nsegs, c)) {
+                for (int r = lane; r < R; r += 32) gptr[r] = grads[int64_t(r) * P + pc.p];
+                __syncwarp();
+            }
+            const ChunkView v = pc.view(c, kBulkChunk, allow_vec);
+            if (v.nbulk == 0) continue;
+            int stop = 0;
+            if (lane == 0) {
+                const uint32_t bytes = uint32_t(v.nbulk * 2);
+                for (int r = 0; r < R; ++r, ++it) {
+                    const int s = int(it % kBulkStages);
+                    const uint32_t phase = uint32_t((it / kBulkStages) & 1);
+                    if (!wait_bounded(&empty[s], phase ^ 1u, timeout_ns, abort, status, 2)) {
+                        stop = 1;
+                        break;
+                    }
+                    if (inject) continue;  // test hook: never signal the stage
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    bulk_g2s(data + int64_t(s) * kBulkChunk * 2, gptr[r] + v.src, bytes, &full[s]);
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+        }
+        // On abort, let the copies already issued land before the CTA's shared memory goes away.
+        // Only the last kBulkStages stage uses can still be in flight, and each is the newest phase
+        // of its stage, so waiting for that phase's parity is exact.
+        if (lane == 0 && *abort && !inject) {
+            const uint64_t drain = globaltimer() + 100000000ull;  // at most 100 ms
+            for (int64_t j = max(int64_t(0), it - kBulkStages); j < it; ++j) {
+                uint64_t* bar = &full[j % kBulkStages];
+                const uint32_t par = uint32_t((j / kBulkStages) & 1);
+                while (!mbar_try_wait(bar, par)) {
+                    if (globaltimer() > drain) {
+                        atomicCAS(status, 0, 4);
+                        break;
+                    }
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------- consumer warps ----------------
+    const int ctid = threadIdx.x;
+    PieceCursor pc;
+    float* shard = nullptr;
+    int64_t it = 0;
+    for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+        if (pc.seek(segs, nsegs, c)) shard = shards[pc.d];
+        const ChunkView v = pc.view(c, kBulkChunk, allow_vec);
+        float* __restrict__ dst = shard + v.dst;
+        if (v.nbulk > 0) {
+            const bool whole = v.nbulk == kBulkChunk;  // every group of the chunk is carried
+            float acc[kGroups][8];
+            for (int r = 0; r < R; ++r, ++it) {
+                const int s = int(it % kBulkStages);
+                const uint32_t phase = uint32_t((it / kBulkStages) & 1);
+                if (!wait_bounded(&full[s], phase, timeout_ns, abort, status, 1)) return;
+                const uint4* row = reinterpret_cast<const uint4*>(data + int64_t(s) * kBulkChunk * 2);
+                if (r == 0) accumulate_row<true, kGroups, kConsumers>(acc, row, ctid, whole, v.nbulk);
+                else accumulate_row<false, kGroups, kConsumers>(acc, row, ctid, whole, v.nbulk);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            const bool wide = (reinterpret_cast<uintptr_t>(dst) & 31u) == 0;  // 32-byte stores possible
+#pragma unroll
+            for (int j = 0; j < kGroups; ++j) {
+                const int64_t e = (int64_t(j) * kConsumers + ctid) * 8;
+                if (whole || e + 8 <= v.nbulk) {
+                    if (wide) {
+                        st_cs_v8(dst + e, acc[j]);
+                    } else {
+                        __stcs(reinterpret_cast<float4*>(dst + e), make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]));
+                        __stcs(reinterpret_cast<float4*>(dst + e + 4), make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]));
+                    }
+                }
+            }
+        }
+        // valid elements not carried by the copies, then padding
+        for (int64_t e = v.nbulk + ctid; e < v.n; e += kConsumers)
+            dst[e] = (e < v.nvalid) ? sum_scalar(grads, R, P, v.p, v.src + e) : 0.0f;
+    }
+}
+
+}  // namespace
+
+size_t bulk_smem_bytes(int R) { return 128 + size_t(kBulkStages) * size_t(kBulkChunk) * 2 + sizeof(void*) * size_t(R); }
+
+cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, int nsegs, int64_t nchunks, const uint16_t* const* grads,
+                                       float* const* shards, int R, int P, int allow_vec, int ctas, int* status,
+                                       uint64_t timeout_ns, int inject, cudaStream_t stream) {
+    if (nchunks <= 0) return cudaSuccess;
+    const size_t smem = bulk_smem_bytes(R);
+    cudaError_t e = cudaFuncSetAttribute(reduce_scatter_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    if (e != cudaSuccess) return e;
+    const int grid = int(std::min<int64_t>(ctas, nchunks));
+    reduce_scatter_bulk_kernel<<<grid, kBulkThreads, smem, stream>>>(segs, nsegs, nchunks, grads, shards, R, P,
+                                                                     allow_vec, status, timeout_ns, inject);
+    return cudaGetLastError();
+}
+
+}  // namespace tide

@@ -50,7 +50,12 @@ struct tide_group {
     int device = 0;
     int sm_count = 0;
     int rs_ctas = 0, ag_ctas = 0;  // 0 = default
+    int rs_variant = TIDE_RS_AUTO;
+    uint64_t timeout_ns = tide::kDefaultTimeoutNs;
+    uint32_t debug = 0;
+    int* d_status = nullptr;  // device status word written by bounded waits that expire
     tide::RsSeg* d_rs = nullptr;
+    tide::RsSeg* d_rs_bulk = nullptr;
     tide::AgSeg* d_ag = nullptr;
     size_t slot_cap = 0;
     Slot slots[kSlots];
@@ -73,6 +78,8 @@ void release(tide_group* g) {
         if (s.dev) cudaFree(s.dev);
     }
     if (g->d_rs) cudaFree(g->d_rs);
+    if (g->d_rs_bulk) cudaFree(g->d_rs_bulk);
+    if (g->d_status) cudaFree(g->d_status);
     if (g->d_ag) cudaFree(g->d_ag);
     delete g;
 }
@@ -126,6 +133,14 @@ int finish_slot(tide_group* g, int k, cudaStream_t stream) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int default_ctas(const tide_group* g, int per_sm) { return std::max(1, g->sm_count * per_sm); }
+
+// Bulk-copy kernel unless the register path is asked for; it needs 16-byte aligned pointers (the
+// register path's element-wise fallback covers the rest).  Measured on GB300 it is the faster of
+// the two at every CTA count, most of all when the count is capped below the SM count.
+bool use_bulk(const tide_group* g, bool aligned) {
+    if (!aligned || g->plan.rs_bulk.empty() || !g->d_rs_bulk) return false;
+    return g->rs_variant != TIDE_RS_REGISTER;
+}
 
 }  // namespace
 
@@ -190,6 +205,14 @@ int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* ro
         e = cudaMemcpy(g->d_rs, rs.data(), rs.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
     if (e == cudaSuccess && !ag.empty())
         e = cudaMemcpy(g->d_ag, ag.data(), ag.size() * sizeof(tide::AgSeg), cudaMemcpyHostToDevice);
+    const auto& rb = g->plan.rs_bulk;
+    if (e == cudaSuccess && !rb.empty()) {
+        e = cudaMalloc(&g->d_rs_bulk, rb.size() * sizeof(tide::RsSeg));
+        if (e == cudaSuccess)
+            e = cudaMemcpy(g->d_rs_bulk, rb.data(), rb.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
+    }
+    if (e == cudaSuccess) e = cudaMalloc(&g->d_status, sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(g->d_status, 0, sizeof(int));
     // a table holds the R*P gradient pointers + R shard pointers (reduce-scatter) or R + P
     // pointers (all-gather)
     g->slot_cap = size_t(R) * P + R + P;
@@ -248,7 +271,8 @@ int tide_group_set_ctas(tide_group_t g, int32_t rs_ctas, int32_t ag_ctas) {
 int tide_group_get_ctas(tide_group_t g, int32_t* rs_ctas, int32_t* ag_ctas) {
     if (!g || !rs_ctas || !ag_ctas) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);
-    *rs_ctas = g->rs_ctas ? g->rs_ctas : default_ctas(g, tide::kRsCtasPerSm);
+    *rs_ctas = g->rs_ctas ? g->rs_ctas
+                          : (g->rs_variant == TIDE_RS_REGISTER ? default_ctas(g, tide::kRsCtasPerSm) : g->sm_count);
     *ag_ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgCtasPerSm);
     return TIDE_OK;
 }
@@ -276,10 +300,19 @@ int tide_reduce_scatter(tide_group_t g, const void* const* grads, void* const* s
     int k = 0;
     if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
     void** dev = g->slots[k].dev;
-    const int ctas = g->rs_ctas ? g->rs_ctas : default_ctas(g, tide::kRsCtasPerSm);
-    const cudaError_t e = tide::launch_reduce_scatter(
-        g->d_rs, int(g->plan.rs.size()), g->plan.rs_chunks, reinterpret_cast<const uint16_t* const*>(dev),
-        reinterpret_cast<float* const*>(dev + size_t(R) * P), R, P, aligned ? 1 : 0, ctas, st);
+    const auto* gp = reinterpret_cast<const uint16_t* const*>(dev);
+    auto* sp = reinterpret_cast<float* const*>(dev + size_t(R) * P);
+    cudaError_t e;
+    if (use_bulk(g, aligned)) {
+        const int ctas = g->rs_ctas ? g->rs_ctas : g->sm_count;
+        e = tide::launch_reduce_scatter_bulk(g->d_rs_bulk, int(g->plan.rs_bulk.size()), g->plan.rs_bulk_chunks, gp, sp,
+                                             R, P, 1, ctas, g->d_status, g->timeout_ns,
+                                             (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
+    } else {
+        const int ctas = g->rs_ctas ? g->rs_ctas : default_ctas(g, tide::kRsCtasPerSm);
+        e = tide::launch_reduce_scatter(g->d_rs, int(g->plan.rs.size()), g->plan.rs_chunks, gp, sp, R, P,
+                                        aligned ? 1 : 0, ctas, st);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return finish_slot(g, k, st);
 }
@@ -364,6 +397,39 @@ int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* p
     }
     g->last_ce_copies = copies;
     g->last_ce_uniform = uniform ? 1 : 0;
+    return TIDE_OK;
+}
+
+int tide_group_set_rs_variant(tide_group_t g, int32_t variant) {
+    if (!g || variant < TIDE_RS_AUTO || variant > TIDE_RS_BULK) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    g->rs_variant = variant;
+    return TIDE_OK;
+}
+
+int tide_group_set_wait_timeout(tide_group_t g, uint64_t timeout_ns) {
+    if (!g) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    g->timeout_ns = timeout_ns ? timeout_ns : tide::kDefaultTimeoutNs;
+    return TIDE_OK;
+}
+
+int tide_group_set_debug(tide_group_t g, uint32_t flags) {
+    if (!g || (flags & ~uint32_t(TIDE_DEBUG_STALL_PRODUCER))) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    g->debug = flags;
+    return TIDE_OK;
+}
+
+int tide_group_device_status(tide_group_t g, int32_t* status) {
+    if (!g || !status) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    int rc = check_device(g);
+    if (rc != TIDE_OK) return rc;
+    int v = 0;
+    TIDE_CUDA(cudaMemcpy(&v, g->d_status, sizeof(int), cudaMemcpyDeviceToHost));
+    if (v) TIDE_CUDA(cudaMemset(g->d_status, 0, sizeof(int)));
+    *status = v;
     return TIDE_OK;
 }
 

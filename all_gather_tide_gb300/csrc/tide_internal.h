@@ -15,6 +15,15 @@ constexpr int kRsUnroll = 2;
 constexpr int64_t kRsChunk = int64_t(kRsThreads) * 8 * kRsUnroll;  // 4096 elements
 constexpr int kRsCtasPerSm = 2;
 
+// Bulk-copy reduce-scatter geometry: 1 producer warp + kBulkConsumerWarps consumer warps, one CTA
+// per SM (16 warps in all), kBulkStages shared-memory stages of one rank row of a kBulkChunk-element
+// chunk (45 KB).
+constexpr int kBulkConsumerWarps = 15;
+constexpr int kBulkThreads = (kBulkConsumerWarps + 1) * 32;
+constexpr int64_t kBulkChunk = 23040;  // 15 warps x 32 threads x 6 groups x 8 elements
+constexpr int kBulkStages = 4;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // bound of every device-side wait
+
 // All-gather placement kernel geometry.
 constexpr int kAgThreads = 256;
 constexpr int kAgUnroll = 4;
@@ -53,6 +62,8 @@ struct Plan {
     int64_t S = 0, U = 0;
     std::vector<RsSeg> rs;
     int64_t rs_chunks = 0;
+    std::vector<RsSeg> rs_bulk;  // same pieces, chunked for the bulk-copy kernel
+    int64_t rs_bulk_chunks = 0;
     std::vector<AgSeg> ag;
     int64_t ag_chunks = 0;
 };
@@ -69,6 +80,11 @@ int record_cuda_error(cudaError_t e);
 cudaError_t launch_reduce_scatter(const RsSeg* segs, int nsegs, int64_t nchunks,
                                   const uint16_t* const* grads, float* const* shards, int R, int P,
                                   int allow_vec, int ctas, cudaStream_t stream);
+// Bulk-copy variant: dynamic shared memory per CTA (stages + the current piece's R pointers).
+size_t bulk_smem_bytes(int R);
+cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, int nsegs, int64_t nchunks, const uint16_t* const* grads,
+                                       float* const* shards, int R, int P, int allow_vec, int ctas, int* status,
+                                       uint64_t timeout_ns, int inject, cudaStream_t stream);
 cudaError_t launch_all_gather(const AgSeg* segs, int nsegs, int64_t nchunks,
                               const uint16_t* const* shards, uint16_t* const* params,
                               int allow_vec, int ctas, cudaStream_t stream);

@@ -200,6 +200,8 @@ def run_tide(args, rank, world, local_rank):
     S, U = layout(g)
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
     G.set_ctas(args.rs_ctas, args.ag_ctas)
+    G.set_rs_variant({"auto": tide.TIDE_RS_AUTO, "register": tide.TIDE_RS_REGISTER,
+                      "bulk": tide.TIDE_RS_BULK}[args.rs_variant])
     rs_ctas, ag_ctas = G.get_ctas()
     buf = Buffers(g, S, dev)
     stream = torch.cuda.Stream(device=dev)
@@ -393,29 +395,35 @@ def cta_sweep(G, buf, stream, args, concurrent):
     between collective speed and interference; Fig. 4 and Table 4 of the paper)."""
     g_rs = rs_bytes_of(G)
     g_ag = 4 * G.U
+    import all_gather_tide_gb300 as tide
+
     rows = []
-    for kind, counts in (("reduce_scatter", args.sweep_rs), ("all_gather_sm", args.sweep_ag)):
-        for n in counts:
-            if kind == "reduce_scatter":
-                G.set_ctas(n, 0)
-                launch = lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream)
-                nbytes, reps = g_rs, 1
-            else:
-                G.set_ctas(0, n)
-                launch = lambda: [G.all_gather(buf.ag_list, buf.params, stream) for _ in range(8)]
-                nbytes, reps = g_ag * 8, 8
-            with torch.cuda.stream(stream):
-                launch()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                launch()
-                e1.record(stream)
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1)
-            c = concurrent(launch, kind, reps=2)
-            rows.append({"kind": kind, "ctas": n, "alone_ms": ms / reps, "gbs": nbytes / (ms * 1e-3) / 1e9,
-                         "gemm_slowdown_pct": c["slowdown_pct"], "gemms": c["gemms_started_inside"]})
+    cases = [("reduce_scatter", v, n) for v in (tide.TIDE_RS_REGISTER, tide.TIDE_RS_BULK) for n in args.sweep_rs]
+    cases += [("all_gather_sm", 0, n) for n in args.sweep_ag]
+    for kind, variant, n in cases:
+        if kind == "reduce_scatter":
+            G.set_ctas(n, 0)
+            G.set_rs_variant(variant)
+            launch = lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream)
+            nbytes, reps = g_rs, 1
+        else:
+            G.set_ctas(0, n)
+            launch = lambda: [G.all_gather(buf.ag_list, buf.params, stream) for _ in range(8)]
+            nbytes, reps = g_ag * 8, 8
+        with torch.cuda.stream(stream):
+            launch()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            launch()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        c = concurrent(launch, kind, reps=2)
+        rows.append({"kind": kind, "variant": {0: "-", 1: "register", 2: "bulk"}[variant], "ctas": n,
+                     "alone_ms": ms / reps, "gbs": nbytes / (ms * 1e-3) / 1e9,
+                     "gemm_slowdown_pct": c["slowdown_pct"], "gemms": c["gemms_started_inside"]})
     G.set_ctas(args.rs_ctas, args.ag_ctas)
+    G.set_rs_variant(tide.TIDE_RS_AUTO)
     return rows
 
 
@@ -557,6 +565,7 @@ def main():
     ap.add_argument("--scale", type=int, default=1, help="divide every dimension by this (profiling cases)")
     ap.add_argument("--rs-ctas", type=int, default=0)
     ap.add_argument("--ag-ctas", type=int, default=0)
+    ap.add_argument("--rs-variant", choices=["auto", "register", "bulk"], default="auto")
     ap.add_argument("--interference-ctas", type=int, nargs="*", default=[16, 32])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-reps", type=int, default=4)

@@ -98,7 +98,8 @@ int tide_group_valid_rows(tide_group_t g, int32_t d, int32_t p, int64_t *v);
 
 /*
  * CTA counts of the reduce-scatter and all-gather kernels.  0 restores the default (enough
- * CTAs to fill every SM); a positive value is used as given (at most the work's chunk count),
+ * CTAs to fill every SM: one per SM for the bulk-copy reduce-scatter, two for the register path,
+ * four for the placement); a positive value is used as given (at most the work's chunk count),
  * so a caller can leave SMs to concurrent compute (Fig. 3, Fig. 4, Table 4).
  */
 int tide_group_set_ctas(tide_group_t g, int32_t rs_ctas, int32_t ag_ctas);
@@ -144,6 +145,35 @@ int tide_all_gather(tide_group_t g, const void *const *shards, void *const *para
  */
 int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *params,
                        void *stream);
+
+/* ---- reduce-scatter kernel variants and device-side waits --------------------------------- */
+#define TIDE_RS_AUTO 0     /* bulk-copy path when every pointer is 16-byte aligned, else register path */
+#define TIDE_RS_REGISTER 1 /* 16-byte register loads of 8 ranks in flight per thread, 2 CTAs per SM */
+#define TIDE_RS_BULK 2     /* 45 KB bulk asynchronous copies, one rank row per stage, 1 CTA per SM */
+
+/*
+ * Chooses the reduce-scatter kernel (Fig. 2b step 5 / Fig. 6a: sums formed by a bounded number of
+ * CTAs fed by bulk copies).  Both give identical bits.  The bulk path needs 16-byte aligned
+ * pointers; otherwise the register path runs.
+ */
+int tide_group_set_rs_variant(tide_group_t g, int32_t variant);
+
+/*
+ * Every device-side wait of the library's kernels (the bulk path's mbarrier waits) gives up after
+ * `timeout_ns` (0 = the default, 2 s): it writes a nonzero code to the group's device status word,
+ * the CTA drains its own copies in flight and returns.  Nothing traps.
+ */
+int tide_group_set_wait_timeout(tide_group_t g, uint64_t timeout_ns);
+
+/* Reads the group's device status word (0 = no wait expired; 1 = a consumer wait expired,
+ * 2 = a producer wait expired, 4 = draining copies after an abort expired) and clears it.
+ * Synchronous: copies from the device. */
+int tide_group_device_status(tide_group_t g, int32_t *status);
+
+/* Test hook: with TIDE_DEBUG_STALL_PRODUCER the bulk path's producer never signals its stages, so
+ * the consumers' bounded waits expire and the status word reports it (no copy is issued). */
+#define TIDE_DEBUG_STALL_PRODUCER 0x1u
+int tide_group_set_debug(tide_group_t g, uint32_t flags);
 
 /* Copies issued by the last tide_all_gather_ce on g, and whether the uniform-pitch form was used. */
 int tide_group_last_ce_copies(tide_group_t g, int64_t *copies, int32_t *uniform_pitch);

@@ -88,7 +88,7 @@ def _ids(gs):
     return [g.name for g in gs]
 
 
-def run_rs(tide, g, ctas=0, misalign=False, flags=0):
+def run_rs(tide, g, ctas=0, misalign=False, flags=0, variant=0):
     lay = oracle.plan(g.R, g.rows, g.row_len)
     host = rng.group_grads(g)
     want = oracle.reduce_scatter(lay, [[t.numpy().view(np.uint16) for t in row] for row in host])
@@ -97,8 +97,10 @@ def run_rs(tide, g, ctas=0, misalign=False, flags=0):
     shards = [Guarded(lay.S, torch.float32, fill=F32_SENTINEL) for _ in range(g.R)]
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
     G.set_ctas(ctas, 0)
+    G.set_rs_variant(variant)
     G.reduce_scatter([[x.view for x in row] for row in grads], [s.view for s in shards])
     torch.cuda.synchronize()
+    assert G.device_status() == 0
     for d in range(g.R):
         got = f32_bits(shards[d].view)
         bad = np.nonzero(got != want[d].view(np.uint32))[0]
@@ -161,6 +163,93 @@ def run_ag(tide, g, ce=False, ctas=0, misalign=False, uniform=True, flags=0):
 @pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
 def test_reduce_scatter_matches_oracle(tide, g):
     run_rs(tide, g)
+
+
+@pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
+def test_reduce_scatter_bulk_matches_oracle(tide, g):
+    run_rs(tide, g, variant=tide.TIDE_RS_BULK)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 16, 24, 152])
+def test_reduce_scatter_bulk_cta_counts(tide, ctas):
+    run_rs(tide, group("qwen3moe").scaled(16), ctas=ctas, variant=tide.TIDE_RS_BULK)
+    run_rs(tide, group("wan_r64").scaled(16), ctas=ctas, variant=tide.TIDE_RS_BULK)
+
+
+SPECIAL_FINITE = [0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x807F, 0x0080, 0x8080, 0x7F7F, 0xFF7F, 0x3F80, 0xBF80,
+                  0x0100, 0x00FF]
+SPECIAL_NONFINITE = [0x7F80, 0xFF80, 0x7FC0]
+
+
+def _special_grads(g, seed, pool):
+    rs = np.random.default_rng(seed)
+    out = []
+    for r in range(g.R):
+        row = []
+        for p in range(g.P):
+            n = g.numel(p)
+            base = rng.grad_bits(g, r, p).numpy().view(np.uint16).copy()
+            pick = rs.random(n) < 0.5
+            base[pick] = np.asarray(pool, np.uint16)[rs.integers(0, len(pool), int(pick.sum()))]
+            row.append(base)
+        out.append(row)
+    for r in range(g.R):  # one element that is -0.0 on every rank: its sum must stay -0.0
+        out[r][-1][0] = 0x8000
+    return out
+
+
+@pytest.mark.parametrize("variant", [1, 2], ids=["register", "bulk"])
+def test_special_values(tide, variant):
+    """Signed zeros, bf16 subnormals (fp32 subnormals after widening), the largest finite values
+    (whose sums overflow to infinity under round-to-nearest), infinities and NaN: finite results
+    bit for bit, NaN where the oracle has NaN."""
+    g = Group("specials", 8, (("a", 640, 64), ("b", 37, 24), ("c", 4099, 1)))
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    for seed, pool in ((1, SPECIAL_FINITE), (2, SPECIAL_FINITE + SPECIAL_NONFINITE)):
+        host = _special_grads(g, seed, pool)
+        want = np.stack(oracle.reduce_scatter(lay, host))
+        dev = [[torch.from_numpy(a.view(np.int16)).cuda() for a in row] for row in host]
+        out = torch.empty(g.R, lay.S, dtype=torch.float32, device="cuda")
+        G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+        G.set_rs_variant(variant)
+        G.reduce_scatter(dev, list(out))
+        torch.cuda.synchronize()
+        got = out.cpu().numpy()
+        nan = np.isnan(want)
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+        if seed == 1:
+            assert np.isinf(want).any() and (want.view(np.uint32) == 0x80000000).any()
+            assert ((np.abs(want) < 1.1754944e-38) & (want != 0)).any()  # fp32 subnormal results
+        G.close()
+
+
+def test_bulk_wait_timeout_reports_status_and_context_survives(tide):
+    """A producer that never signals (test hook) makes the bounded waits expire (the consumers'
+    on data that never arrives, the producer's on stages never freed): the kernel returns, the
+    status word records the first wait that gave up, and the next call runs normally."""
+    g = group("llama70b").scaled(64)
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+    G.set_rs_variant(tide.TIDE_RS_BULK)
+    G.set_ctas(8, 0)
+    G.set_wait_timeout(50_000_000)  # 50 ms
+    grads = [[rng.grad_bits(g, r, p, device="cuda").view(torch.bfloat16) for p in range(g.P)] for r in range(g.R)]
+    shards = torch.zeros(g.R, G.S, dtype=torch.float32, device="cuda")
+    G.set_debug(tide.TIDE_DEBUG_STALL_PRODUCER)
+    G.reduce_scatter(grads, list(shards))
+    torch.cuda.synchronize()
+    # both sides wait on stages nobody fills or frees; whichever bound expires first is recorded
+    assert G.device_status() in (1, 2)
+    G.set_debug(0)
+    G.set_wait_timeout(0)
+    G.reduce_scatter(grads, list(shards))
+    torch.cuda.synchronize()
+    assert G.device_status() == 0
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    want = oracle.reduce_scatter(lay, [[t.view(torch.int16).cpu().numpy().view(np.uint16) for t in row]
+                                       for row in grads])
+    assert np.array_equal(f32_bits(shards), np.stack(want).view(np.uint32))
+    G.close()
 
 
 @pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
@@ -278,16 +367,23 @@ def _sample_positions(lay, seed, n=3000):
     return np.asarray(d, np.int64), np.asarray(j, np.int64)
 
 
-@pytest.mark.parametrize("name", FULL)
-def test_full_size_reduce_scatter(tide, name):
+FULL_CASES = [(n, 0) for n in FULL] + [("llama70b", 16), ("qwen3moe", 16), ("wan_r64", 24)]
+
+
+@pytest.mark.parametrize("name,ctas", FULL_CASES, ids=[f"{n}-ctas{c or 'default'}" for n, c in FULL_CASES])
+def test_full_size_reduce_scatter(tide, name, ctas):
+    """Default CTAs = the benchmark's step; capped CTAs = the automatic bulk-copy path the
+    interference harness times."""
     g = group(name)
     lay = oracle.plan(g.R, g.rows, g.row_len)
     grads = [[rng.grad_bits(g, r, p, device="cuda").view(torch.bfloat16) for p in range(g.P)] for r in range(g.R)]
     shards = torch.empty(g.R, lay.S, dtype=torch.float32, device="cuda")
     shards.view(torch.int32).fill_(F32_SENTINEL)
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+    G.set_ctas(ctas, 0)
     G.reduce_scatter(grads, list(shards))
     torch.cuda.synchronize()
+    assert G.device_status() == 0
     # (1) sampled outputs, computed one by one by the oracle from regenerated inputs
     d, j = _sample_positions(lay, seed=len(name))
     want = oracle.rs_points(lay, d, j, lambda r, p, idx: rng.grad_bits(g, r, p, idx=torch.from_numpy(idx))
