@@ -59,6 +59,9 @@ SIGNATURES = {
     "tide_group_device_status": (ctypes.c_int, [_vp, _i32p]),
     "tide_group_set_debug": (ctypes.c_int, [_vp, ctypes.c_uint32]),
     "tide_reduce_scatter_noalloc": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, _i64p, _i64p, _vpp, _vpp, _vp]),
+    "tide_probe_hold": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64,
+                                       _vp, _vp]),
+    "tide_probe_bulk_read": (ctypes.c_int, [_vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]),
     "tide_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "tide_last_cuda_error": (ctypes.c_int, []),
     "tide_version": (ctypes.c_int, []),
@@ -243,6 +246,20 @@ def tide_group_last_ce_copies(g: int) -> Tuple[int, bool]:
     n, u = ctypes.c_int64(), ctypes.c_int32()
     _check(lib().tide_group_last_ce_copies(g, ctypes.byref(n), ctypes.byref(u)), "tide_group_last_ce_copies")
     return n.value, bool(u.value)
+
+
+def tide_probe_hold(ctas: int, threads: int, smem_bytes: int, cluster_size: int, hold_ns: int, records=None,
+                    stream=None) -> None:
+    """Resident probe CTAs (Fig. 4 spin kernels; Table 5 SM-id probe when ``records`` is given:
+    a device uint64 tensor of 3*ctas entries receiving SM id, entry and exit ns per CTA)."""
+    _check(lib().tide_probe_hold(ctas, threads, smem_bytes, cluster_size, hold_ns,
+                                 _ptr(records) if records is not None else None, _stream(stream)), "tide_probe_hold")
+
+
+def tide_probe_bulk_read(buf, nbytes: int, ctas: int, copy_bytes: int, stages: int, out, stream=None) -> None:
+    """Bulk-copy read bandwidth probe; ``out`` is a device uint32/int32 tensor of 2 entries."""
+    _check(lib().tide_probe_bulk_read(_ptr(buf), nbytes, ctas, copy_bytes, stages, _ptr(out), _stream(stream)),
+           "tide_probe_bulk_read")
 
 
 # ---- convenience object -----------------------------------------------------------------------

@@ -165,19 +165,6 @@ struct ChunkView {
     int d, p;
 };
 
-__device__ __forceinline__ ChunkView view_of(const RsSeg& sg, int64_t c, int64_t chunk, int allow_vec) {
-    ChunkView v;
-    const int64_t base = (c - sg.chunk_begin) * chunk;
-    v.n = min(chunk, sg.total - base);
-    v.nvalid = max(int64_t(0), min(v.n, sg.valid - base));
-    v.nbulk = (allow_vec && sg.vec) ? (v.nvalid & ~int64_t(7)) : 0;
-    v.src = sg.src_off + base;
-    v.dst = sg.dst_off + base;
-    v.d = sg.d;
-    v.p = sg.p;
-    return v;
-}
-
 constexpr uint64_t kTimerCheckEvery = 256;
 
 // Wait for the phase of `bar` with the given parity, for at most `timeout_ns` from the first

@@ -275,15 +275,24 @@ def run_tide(args, rank, world, local_rank):
         "legs": legs,
         "gpu_launches": 2 * args.steps,
     }
-    traffic = recorded_traffic("reduce_scatter_kernel", g.name, ["rs_kernel.cu", "tide_internal.h"])
-    out["roofline"] = {"bound": "hbm", "kernel": "reduce_scatter_kernel", "achieved": legs["reduce_scatter"]["gbs"],
+    if args.rs_variant == "register":
+        rs_kernel, rs_srcs = "reduce_scatter_kernel", ["rs_kernel.cu", "tide_internal.h"]
+    else:  # 16-byte aligned torch allocations: the bulk-copy kernel runs
+        rs_kernel, rs_srcs = "reduce_scatter_bulk_kernel", ["rs_bulk_kernel.cu", "tide_internal.h"]
+    legs["reduce_scatter"]["kernel"] = rs_kernel
+    traffic = recorded_traffic(rs_kernel, g.name, rs_srcs)
+    out["roofline"] = {"bound": "hbm", "kernel": rs_kernel, "achieved": legs["reduce_scatter"]["gbs"],
                        "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                        "frac": legs["reduce_scatter"]["gbs"] / peak, "traffic": traffic,
                        "algorithmic_bytes": b_rs}
     out["clocks"] = clocks.summary()
 
+    if not args.no_stock and rank == 0:
+        out["stock_comparator"] = stock_comparator(G, g, buf, S, U, stream, legs)
     if not args.no_interference and rank == 0:
         out["interference"] = interference(G, buf, stream, dev, args)
+    if args.probes and rank == 0:
+        out["probes"] = probes(G, buf, stream, dev, args)
     if not args.no_e2e:
         out["e2e"] = end_to_end(G, g, buf, S, U, dev, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -307,6 +316,72 @@ def time_ce(G, buf, stream, b_ag, iters):
     avg = statistics.mean(ms)
     return {"gbs": b_ag / (avg * 1e-3) / 1e9, "ms": avg, "ms_median": statistics.median(ms), "bytes": b_ag,
             "copies": copies, "uniform_pitch": uniform, "ctas": 0}
+
+
+# ---- one-GPU "stock" comparator ----------------------------------------------------------------
+
+
+def stock_comparator(G, g, buf, S, U, stream, legs):
+    """The layout-converting path the paper compares against (Table 1 "Full-group pack", Table 7
+    "+ Copy-out", Table 8 "FSDP2 columns include _chunk_cat"), emulated on one GPU with plain
+    PyTorch ops: every contributor packs its per-parameter bf16 gradients into a full-group fp32
+    buffer ([R, S] per contributor, zero padding; torch._chunk_cat as FSDP2 does), the packed
+    buffers are summed per destination (the reduce-scatter), and the all-gather output, a flat
+    rank-major buffer, is copied out into padded per-parameter storage (split_with_sizes_copy).
+    Timed with CUDA events; reported against the same algorithmic bytes as the direct path."""
+    R, P = g.R, g.P
+    m = [(r + R - 1) // R for r in g.rows]  # padded rows (the comparator's own arithmetic)
+    sizes = [m[p] * g.row_len[p] for p in range(P)]
+    packed = torch.empty(R, R, S, dtype=torch.float32, device=buf.shards.device)
+    out_shards = torch.empty(R, S, dtype=torch.float32, device=buf.shards.device)
+    padded = [torch.empty(R, sizes[p], dtype=torch.bfloat16, device=buf.shards.device) for p in range(P)]
+    views = [[buf.grads[r][p].view(g.rows[p], g.row_len[p]) for p in range(P)] for r in range(R)]
+    have_chunk_cat = hasattr(torch, "_chunk_cat")
+
+    def pack(r):
+        if have_chunk_cat:
+            torch._chunk_cat(views[r], 0, R, out=packed[r])
+        else:  # same layout by hand: chunk d of every parameter, zero-padded, concatenated
+            packed[r].zero_()
+            for p in range(P):
+                for d, piece in enumerate(torch.chunk(views[r][p], R, dim=0)):
+                    o = sum(sizes[:p])
+                    packed[r, d, o:o + piece.numel()].copy_(piece.reshape(-1))
+
+    def rs():
+        for r in range(R):
+            pack(r)
+        torch.sum(packed, dim=0, out=out_shards)
+
+    def ag():
+        torch.split_with_sizes_copy(buf.ag_in.view(R, S), sizes, dim=1, out=padded)
+
+    def timed(fn, reps=3):
+        with torch.cuda.stream(stream):
+            fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    rs_ms, ag_ms = timed(rs), timed(ag)
+    b_rs, b_ag = rs_bytes(g, S, U), ag_bytes(U)
+    res = {
+        "reduce_scatter": {"ms": rs_ms, "gbs_of_direct_bytes": b_rs / (rs_ms * 1e-3) / 1e9,
+                           "direct_ms": legs["reduce_scatter"]["ms"], "speedup_direct": rs_ms / legs["reduce_scatter"]["ms"],
+                           "extra_buffer_bytes": packed.numel() * 4, "pack": "torch._chunk_cat" if have_chunk_cat else "chunk+copy"},
+        "all_gather_copy_out": {"ms": ag_ms, "gbs_of_direct_bytes": b_ag / (ag_ms * 1e-3) / 1e9,
+                                "direct_ms": legs["all_gather_sm"]["ms"], "speedup_direct": ag_ms / legs["all_gather_sm"]["ms"],
+                                "op": "torch.split_with_sizes_copy into padded [R, m_p*L_p] storage"},
+    }
+    err = (out_shards - buf.shards).abs().max().item()
+    res["reduce_scatter"]["max_abs_diff_vs_direct"] = err
+    del packed, out_shards, padded
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---- interference harness ----------------------------------------------------------------------
@@ -431,51 +506,227 @@ def rs_bytes_of(G) -> int:
     return G.R * G.U * 2 + G.R * G.S * 4
 
 
+# ---- interference probes: spin-CTA curve, SM-id probe, victims of Table 4 ---------------------
+
+
+def _window_times(launch_a, b_stream, victim, n_victims, a_stream):
+    """Launch `launch_a` on a_stream and n_victims victims back to back on b_stream from the same
+    start; returns (a's elapsed ms, victim ms list for victims that started inside a's window)."""
+    torch.cuda.synchronize()
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(a_stream)
+    with torch.cuda.stream(a_stream):
+        launch_a()
+    s1.record(a_stream)
+    b_stream.wait_event(s0)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_victims)]
+    with torch.cuda.stream(b_stream):
+        for e in ev:
+            e[0].record(b_stream)
+            victim()
+            e[1].record(b_stream)
+    torch.cuda.synchronize()
+    end = s0.elapsed_time(s1)
+    inside = [e[0].elapsed_time(e[1]) for e in ev if 0 <= s0.elapsed_time(e[0]) < end]
+    return end, inside
+
+
+def probes(G, buf, stream, dev, args):
+    """Fig. 4 (GEMM slowdown vs resident spin CTAs), Table 5 (SM-id probe: probe CTAs displaced past
+    the first wave and SMs held by the collective) and Table 4 (slowdown of a 1-wave GEMM, a 28-wave
+    GEMM and an elementwise kernel beside the reduce-scatter), on one GB300."""
+    import all_gather_tide_gb300 as tide
+
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    vs = torch.cuda.Stream(device=dev)
+    a1 = torch.randn(4096, 8192, device=dev, dtype=torch.bfloat16)
+    b1 = torch.randn(8192, 4096, device=dev, dtype=torch.bfloat16)
+    c1 = torch.empty(4096, 4096, device=dev, dtype=torch.bfloat16)
+    a2 = torch.randn(16384, 8192, device=dev, dtype=torch.bfloat16)
+    b2 = torch.randn(8192, 8192, device=dev, dtype=torch.bfloat16)
+    c2 = torch.empty(16384, 8192, device=dev, dtype=torch.bfloat16)
+    x = torch.randn(1 << 28, device=dev)
+    y = torch.randn(1 << 28, device=dev)
+    z = torch.empty(1 << 28, device=dev)
+    victims = {
+        "gemm_1wave_4096x4096x8192": lambda: torch.matmul(a1, b1, out=c1),
+        "gemm_28wave_16384x8192x8192": lambda: torch.matmul(a2, b2, out=c2),
+        "elementwise_add_1GiB": lambda: torch.add(x, y, out=z),
+    }
+
+    def alone(fn, n=20):
+        with torch.cuda.stream(vs):
+            for _ in range(3):
+                fn()
+            ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+            for e in ev:
+                e[0].record(vs)
+                fn()
+                e[1].record(vs)
+        torch.cuda.synchronize()
+        return statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+
+    t_alone = {k: alone(f) for k, f in victims.items()}
+    out = {"sms": sms, "victims_alone_ms": t_alone}
+
+    # Fig. 4: resident CTAs that fill an SM each (the whole register file and 213 KB of shared
+    # memory, like a GEMM CTA)
+    curve = []
+    g1 = victims["gemm_1wave_4096x4096x8192"]
+    for n in args.spin_ctas:
+        hold = lambda: tide.tide_probe_hold(n, 1024, 213 * 1024, 1, 20_000_000, None, stream)
+        _, inside = _window_times(hold, vs, g1, 64, stream)
+        curve.append({"resident_ctas": n, "gemms": len(inside),
+                      "slowdown_pct": 100 * (statistics.median(inside) / t_alone["gemm_1wave_4096x4096x8192"] - 1)
+                      if inside else None})
+    out["spin_curve"] = curve
+
+    # Table 4 / Table 5 for several reduce-scatter configurations
+    configs = [("bulk", 0), ("bulk", 16), ("bulk", 4), ("register", 16)]
+    rows = []
+    recs = torch.zeros(3 * sms, dtype=torch.int64, device=dev)
+    for variant, ctas in configs:
+        G.set_ctas(ctas, 0)
+        G.set_rs_variant(tide.TIDE_RS_BULK if variant == "bulk" else tide.TIDE_RS_REGISTER)
+        rs = lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream)
+        row = {"variant": variant, "ctas": ctas or G.get_ctas()[0]}
+        for name, fn in victims.items():
+            ms, inside = _window_times(rs, vs, fn, 48, stream)
+            row["rs_ms"] = ms
+            row[name] = 100 * (statistics.median(inside) / t_alone[name] - 1) if inside else None
+        # SM-id probes: 32 four-CTA clusters (the GEMM's shape) and one CTA per SM, 50 us each,
+        # launched repeatedly while the reduce-scatter runs
+        disp, res = [], []
+        for shape in ("clusters", "per_sm"):
+            n, cl = (128, 4) if shape == "clusters" else (sms, 1)
+            launches = []
+
+            def probe_many():
+                for _ in range(6):
+                    tide.tide_probe_hold(n, 1024, 213 * 1024, cl, 50_000, recs, vs)
+                    launches.append(recs[:3 * n].clone().view(n, 3))
+
+            torch.cuda.synchronize()
+            s0 = torch.cuda.Event()
+            s0.record(stream)
+            with torch.cuda.stream(stream):
+                rs()
+            vs.wait_event(s0)
+            with torch.cuda.stream(vs):
+                probe_many()
+            torch.cuda.synchronize()
+            for rec in launches:
+                entry = rec[:, 1].double()
+                late = int((entry > entry.min() + 25_000).sum())  # started after the first wave
+                (disp if shape == "clusters" else res).append(late)
+        row["probe_displaced_ctas_mode"] = statistics.mode(disp)
+        row["probe_windows_hit_pct"] = 100.0 * sum(d > 0 for d in disp) / len(disp)
+        row["probe_resident_ctas_mean"] = statistics.mean(res)
+        rows.append(row)
+    G.set_ctas(args.rs_ctas, args.ag_ctas)
+    G.set_rs_variant(tide.TIDE_RS_AUTO)
+    out["table4_table5"] = rows
+    del a2, b2, c2, x, y, z
+    torch.cuda.empty_cache()
+    return out
+
+
 # ---- end to end with host buffers --------------------------------------------------------------
 
 
 def end_to_end(G, g, buf, S, U, dev, args, world):
-    """Same step through the public API, with the inputs copied in from pinned host memory and
-    the outputs copied back every step, inside the timed region."""
+    """Same step through the public API with host buffers: every step copies all its inputs in
+    from pinned host memory and all its outputs back, inside the timed region.  Input copies are
+    spread over several streams (several copy engines), and step k+1's input copies overlap step
+    k's output copies (opposite directions of the host link); events keep every buffer's reuse
+    ordered after its last reader."""
     h_grads = [[t.to("cpu").pin_memory() for t in row] for row in buf.grads]
     h_ag = buf.ag_in.to("cpu").pin_memory()
     h_shards = torch.empty(g.R, S, dtype=torch.float32).pin_memory()
     h_params = [torch.empty(g.numel(p), dtype=torch.bfloat16).pin_memory() for p in range(g.P)]
-    stream = torch.cuda.Stream(device=dev)
     h2d = sum(t.numel() * 2 for row in h_grads for t in row) + h_ag.numel() * 2
     d2h = h_shards.numel() * 4 + sum(t.numel() * 2 for t in h_params)
+    n_in = 4
+    s_in = [torch.cuda.Stream(device=dev) for _ in range(n_in)]
+    s_c = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+    pairs_in = [(buf.grads[r][p], h_grads[r][p]) for r in range(g.R) for p in range(g.P)] + [(buf.ag_in, h_ag)]
+    pairs_in.sort(key=lambda x: -x[0].numel())
+    lanes = [[] for _ in range(n_in)]
+    load = [0] * n_in
+    for d_t, h_t in pairs_in:  # balance the bytes over the input streams
+        k = load.index(min(load))
+        lanes[k].append((d_t, h_t))
+        load[k] += d_t.numel()
+    pairs_out = [(h_shards, buf.shards)] + [(h_params[p], buf.params[p]) for p in range(g.P)]
+    state = {"computed": None, "copied_out": None}
 
     def step():
-        for r in range(g.R):
-            for p in range(g.P):
-                buf.grads[r][p].copy_(h_grads[r][p], non_blocking=True)
-        buf.ag_in.copy_(h_ag, non_blocking=True)
-        G.reduce_scatter(buf.grads, buf.shard_list, stream)
-        G.all_gather(buf.ag_list, buf.params, stream)
-        h_shards.copy_(buf.shards, non_blocking=True)
-        for p in range(g.P):
-            h_params[p].copy_(buf.params[p], non_blocking=True)
+        for k in range(n_in):
+            if state["computed"] is not None:
+                s_in[k].wait_event(state["computed"])  # the previous step's kernels have read the inputs
+            with torch.cuda.stream(s_in[k]):
+                for d_t, h_t in lanes[k]:
+                    d_t.copy_(h_t, non_blocking=True)
+        for k in range(n_in):
+            s_c.wait_stream(s_in[k])
+        if state["copied_out"] is not None:
+            s_c.wait_event(state["copied_out"])  # the previous step's outputs have been copied out
+        G.reduce_scatter(buf.grads, buf.shard_list, s_c)
+        G.all_gather(buf.ag_list, buf.params, s_c)
+        computed = torch.cuda.Event()
+        computed.record(s_c)
+        s_out.wait_event(computed)
+        with torch.cuda.stream(s_out):
+            for h_t, d_t in pairs_out:
+                h_t.copy_(d_t, non_blocking=True)
+        copied_out = torch.cuda.Event()
+        copied_out.record(s_out)
+        state["computed"], state["copied_out"] = computed, copied_out
+
+    def one_direction(direction):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s_c)
+        for k in range(n_in):
+            s_in[k].wait_event(e0)
+            with torch.cuda.stream(s_in[k]):
+                for d_t, h_t in lanes[k]:
+                    if direction == "h2d":
+                        d_t.copy_(h_t, non_blocking=True)
+                    else:
+                        h_t.copy_(d_t, non_blocking=True)
+        for k in range(n_in):
+            s_c.wait_stream(s_in[k])
+        e1.record(s_c)
+        torch.cuda.synchronize()
+        return h2d / (e0.elapsed_time(e1) * 1e-3) / 1e9
 
     steps = max(2, min(args.steps, args.e2e_steps))
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            step()
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            step()
-        e1.record(stream)
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    state["computed"] = state["copied_out"] = None
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_c)
+    for k in range(n_in):
+        s_in[k].wait_event(e0)
+    for _ in range(steps):
+        step()
+    s_c.wait_stream(s_out)
+    e1.record(s_c)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     value = whole_job_gbs(rs_bytes(g, S, U) + ag_bytes(U), steps, world, ms)
+    link = {"h2d_gbs_inputs_only": one_direction("h2d"), "d2h_gbs_same_bytes": one_direction("d2h")}
     del h_grads, h_ag, h_shards, h_params
     return {"value": value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "ms_per_step": ms / steps,
-            "how": "pinned host -> device copies of all inputs, tide_reduce_scatter + tide_all_gather, "
-                   "device -> pinned host copies of all outputs, every step, one stream"}
+            "steps": steps, "ms_per_step": ms / steps, "host_link": link,
+            "how": "pinned host -> device copies of all inputs (4 streams), tide_reduce_scatter + "
+                   "tide_all_gather, device -> pinned host copies of all outputs, every step; step k+1's "
+                   "input copies overlap step k's output copies"}
 
 
 # ---- the host oracle ---------------------------------------------------------------------------
@@ -572,8 +823,11 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="CTA-count sweep of bandwidth vs GEMM slowdown")
     ap.add_argument("--sweep-rs", type=int, nargs="*", default=[8, 16, 20, 24, 32, 48, 64, 96, 152, 304])
     ap.add_argument("--sweep-ag", type=int, nargs="*", default=[8, 16, 24, 32, 64, 152, 608])
+    ap.add_argument("--probes", action="store_true", help="spin-CTA curve, SM-id probe and Table 4 victims")
+    ap.add_argument("--spin-ctas", type=int, nargs="*", default=[1, 4, 8, 12, 16, 20, 24, 32, 48, 64, 96, 152])
     ap.add_argument("--no-interference", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-stock", action="store_true", help="skip the one-GPU pack/copy-out comparator")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

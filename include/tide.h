@@ -209,6 +209,28 @@ int tide_group_last_ce_copies(tide_group_t g, int64_t *copies, int32_t *uniform_
 int tide_reduce_scatter_noalloc(int32_t R, int32_t P, const int64_t *rows, const int64_t *row_len,
                                 const void *const *grads, void *const *shards, void *stream);
 
+/* ---- interference probes (measurement kernels of the interference harness) ----------------- */
+/*
+ * tide_probe_hold — launches `ctas` CTAs of `threads` threads, each claiming `smem_bytes` of
+ * dynamic shared memory (so a large value keeps one CTA per SM, like a GEMM CTA), in clusters of
+ * `cluster_size` (1..8), that keep their SM for `hold_ns` (<= 10 s).  Fig. 4's resident spin
+ * kernels and Table 5's SM-id probe: with `records` (device, 3*ctas uint64) each CTA writes its
+ * SM id, entry and exit %globaltimer values, so CTAs that could not start in the first wave are
+ * visible.  Asynchronous on `stream`; TIDE_EINVAL on bad sizes.
+ */
+int tide_probe_hold(int32_t ctas, int32_t threads, int32_t smem_bytes, int32_t cluster_size, uint64_t hold_ns,
+                    uint64_t *records, void *stream);
+
+/*
+ * tide_probe_bulk_read — reads `bytes` of `buf` (16-byte aligned, device) with `ctas` CTAs, each
+ * streaming `copy_bytes` bulk copies (multiple of 16) through `stages` shared-memory slots
+ * (copy_bytes*stages <= 200 KB).  Measures how an SM's bulk-copy bandwidth depends on the copy
+ * size.  out (device, 2 uint32): out[0] = XOR checksum of the first word of every copy, out[1] =
+ * nonzero if a bounded wait (1 s) expired.
+ */
+int tide_probe_bulk_read(const void *buf, int64_t bytes, int32_t ctas, int32_t copy_bytes, int32_t stages,
+                         uint32_t *out, void *stream);
+
 /* ---- errors ------------------------------------------------------------------------------ */
 const char *tide_strerror(int status);
 /* cudaError_t code of the last CUDA failure reported as TIDE_ECUDA on this host thread. */

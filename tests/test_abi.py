@@ -98,3 +98,13 @@ def test_null_group_calls(tide):
     v = ctypes.c_int64()
     assert L.tide_group_shard_elems(None, ctypes.byref(v)) == tide.TIDE_EINVAL
     assert L.tide_group_destroy(None) == tide.TIDE_OK
+
+
+def test_probe_argument_checks_before_cuda(tide):
+    L = tide.lib()
+    assert L.tide_probe_hold(0, 128, 0, 1, 1000, None, None) == tide.TIDE_EINVAL
+    assert L.tide_probe_hold(6, 128, 0, 4, 1000, None, None) == tide.TIDE_EINVAL  # not whole clusters
+    assert L.tide_probe_hold(4, 2048, 0, 1, 1000, None, None) == tide.TIDE_EINVAL
+    assert L.tide_probe_bulk_read(None, 1024, 1, 4096, 4, None, None) == tide.TIDE_EINVAL
+    assert L.tide_probe_bulk_read(16, 1024, 1, 4095, 4, 16, None) == tide.TIDE_EINVAL
+    assert L.tide_probe_bulk_read(16, 1024, 1, 65536, 4, 16, None) == tide.TIDE_EINVAL  # > 200 KB staged

@@ -1,0 +1,45 @@
+"""The interference probes (resident-CTA / SM-id probe, bulk-copy read probe) on the GPU."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tide():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import all_gather_tide_gb300 as t
+
+    t.lib()
+    return t
+
+
+def test_hold_probe_records_sm_ids_and_times(tide):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n = 8
+    rec = torch.zeros(3 * n, dtype=torch.int64, device="cuda")
+    tide.tide_probe_hold(n, 1024, 213 * 1024, 4, 200_000, rec)
+    torch.cuda.synchronize()
+    r = rec.view(n, 3).cpu().numpy()
+    assert np.all((r[:, 0] >= 0) & (r[:, 0] < sms))
+    assert np.all(r[:, 2] - r[:, 1] >= 200_000)
+    # each CTA fills an SM, and 8 fit at once: 8 different SMs, all started together
+    assert len(set(r[:, 0].tolist())) == n
+    assert r[:, 1].max() - r[:, 1].min() < 150_000
+
+
+def test_bulk_read_probe_checksum(tide):
+    nbytes = 256 << 20
+    copy = 49152
+    buf = torch.randint(-2**31, 2**31 - 1, (nbytes // 4,), dtype=torch.int32, device="cuda")
+    out = torch.zeros(2, dtype=torch.int32, device="cuda")
+    tide.tide_probe_bulk_read(buf, nbytes, 16, copy, 4, out)
+    torch.cuda.synchronize()
+    nchunk = nbytes // copy
+    firsts = buf.view(-1)[: nchunk * copy // 4].view(nchunk, copy // 4)[:, 0].cpu().numpy().view(np.uint32)
+    want = np.bitwise_xor.reduce(firsts)
+    got = out.cpu().numpy().view(np.uint32)
+    assert got[1] == 0
+    assert got[0] == want
