@@ -28,9 +28,13 @@ TIDE_ENOMEM = -5
 TIDE_ERANGE = -6
 TIDE_FLAG_VEC_STRICT = 0x1
 TIDE_FLAG_CE_STRICT = 0x2
+TIDE_FLAG_CE_1D = 0x4
 TIDE_RS_AUTO = 0
 TIDE_RS_REGISTER = 1
 TIDE_RS_BULK = 2
+TIDE_AG_AUTO = 0
+TIDE_AG_REGISTER = 1
+TIDE_AG_BULK = 2
 TIDE_DEBUG_STALL_PRODUCER = 0x1
 
 _lib = None
@@ -55,6 +59,7 @@ SIGNATURES = {
     "tide_all_gather_ce": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_group_last_ce_copies": (ctypes.c_int, [_vp, _i64p, _i32p]),
     "tide_group_set_rs_variant": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "tide_group_set_ag_variant": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "tide_group_set_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_uint64]),
     "tide_group_device_status": (ctypes.c_int, [_vp, _i32p]),
     "tide_group_set_debug": (ctypes.c_int, [_vp, ctypes.c_uint32]),
@@ -62,6 +67,7 @@ SIGNATURES = {
     "tide_probe_hold": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64,
                                        _vp, _vp]),
     "tide_probe_bulk_read": (ctypes.c_int, [_vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]),
+    "tide_stage_into_slots": (ctypes.c_int, [_vp, _vpp, _vpp, ctypes.c_int64, _vpp, _vp]),
     "tide_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "tide_last_cuda_error": (ctypes.c_int, []),
     "tide_version": (ctypes.c_int, []),
@@ -218,6 +224,10 @@ def tide_group_set_rs_variant(g: int, variant: int) -> None:
     _check(lib().tide_group_set_rs_variant(g, variant), "tide_group_set_rs_variant")
 
 
+def tide_group_set_ag_variant(g: int, variant: int) -> None:
+    _check(lib().tide_group_set_ag_variant(g, variant), "tide_group_set_ag_variant")
+
+
 def tide_group_set_wait_timeout(g: int, timeout_ns: int) -> None:
     _check(lib().tide_group_set_wait_timeout(g, timeout_ns), "tide_group_set_wait_timeout")
 
@@ -240,6 +250,16 @@ def tide_reduce_scatter_noalloc(R: int, rows: Sequence[int], row_len: Sequence[i
     _check(lib().tide_reduce_scatter_noalloc(R, len(rows), _i64_array(rows), _i64_array(row_len),
                                              _ptr_array(_flat_grads(grads)), _ptr_array(shards), _stream(stream)),
            "tide_reduce_scatter_noalloc")
+
+
+def tide_stage_into_slots(g: int, grads, slots: Sequence, slot_elems: int, stream=None) -> List[int]:
+    """Slot-Reuse staging: copies every rank's gradients into its slot (packed, no padding) and
+    returns the R*P staged device addresses (flat, index r*P+p) for ``tide_reduce_scatter``."""
+    flat = _flat_grads(grads)
+    staged = (ctypes.c_void_p * len(flat))()
+    _check(lib().tide_stage_into_slots(g, _ptr_array(flat), _ptr_array(slots), slot_elems, staged, _stream(stream)),
+           "tide_stage_into_slots")
+    return [int(x) for x in staged]
 
 
 def tide_group_last_ce_copies(g: int) -> Tuple[int, bool]:
@@ -318,8 +338,14 @@ class Group:
     def last_ce_copies(self) -> Tuple[int, bool]:
         return tide_group_last_ce_copies(self.handle)
 
+    def stage_into_slots(self, grads, slots, slot_elems: int, stream=None) -> List[int]:
+        return tide_stage_into_slots(self.handle, grads, slots, slot_elems, stream)
+
     def set_rs_variant(self, variant: int) -> None:
         tide_group_set_rs_variant(self.handle, variant)
+
+    def set_ag_variant(self, variant: int) -> None:
+        tide_group_set_ag_variant(self.handle, variant)
 
     def set_wait_timeout(self, timeout_ns: int) -> None:
         tide_group_set_wait_timeout(self.handle, timeout_ns)

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libtide.so")
-SOURCES = ["plan.cpp", "tide_api.cpp", "rs_kernel.cu", "rs_bulk_kernel.cu", "ag_kernel.cu", "noalloc.cu", "probes.cu"]
+SOURCES = ["plan.cpp", "tide_api.cpp", "rs_kernel.cu", "rs_bulk_kernel.cu", "ag_kernel.cu", "ag_bulk_kernel.cu", "noalloc.cu", "probes.cu"]
 HEADERS = [os.path.join(CSRC, "tide_internal.h"), os.path.join(ROOT, "include", "tide.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

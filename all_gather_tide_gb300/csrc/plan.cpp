@@ -105,6 +105,15 @@ void make_work_lists(Plan* pl) {
         }
     }
     pl->ag_chunks = chunks;
+
+    pl->ag_bulk.clear();
+    chunks = 0;
+    for (AgSeg sg : pl->ag) {
+        sg.chunk_begin = chunks;
+        chunks += (sg.len + kAgBulkChunk - 1) / kAgBulkChunk;
+        pl->ag_bulk.push_back(sg);
+    }
+    pl->ag_bulk_chunks = chunks;
 }
 
 }  // namespace tide

@@ -51,11 +51,13 @@ struct tide_group {
     int sm_count = 0;
     int rs_ctas = 0, ag_ctas = 0;  // 0 = default
     int rs_variant = TIDE_RS_AUTO;
+    int ag_variant = TIDE_AG_AUTO;
     uint64_t timeout_ns = tide::kDefaultTimeoutNs;
     uint32_t debug = 0;
     int* d_status = nullptr;  // device status word written by bounded waits that expire
     tide::RsSeg* d_rs = nullptr;
     tide::RsSeg* d_rs_bulk = nullptr;
+    tide::AgSeg* d_ag_bulk = nullptr;
     tide::AgSeg* d_ag = nullptr;
     size_t slot_cap = 0;
     Slot slots[kSlots];
@@ -79,6 +81,7 @@ void release(tide_group* g) {
     }
     if (g->d_rs) cudaFree(g->d_rs);
     if (g->d_rs_bulk) cudaFree(g->d_rs_bulk);
+    if (g->d_ag_bulk) cudaFree(g->d_ag_bulk);
     if (g->d_status) cudaFree(g->d_status);
     if (g->d_ag) cudaFree(g->d_ag);
     delete g;
@@ -211,6 +214,12 @@ int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* ro
         if (e == cudaSuccess)
             e = cudaMemcpy(g->d_rs_bulk, rb.data(), rb.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
     }
+    const auto& ab = g->plan.ag_bulk;
+    if (e == cudaSuccess && !ab.empty()) {
+        e = cudaMalloc(&g->d_ag_bulk, ab.size() * sizeof(tide::AgSeg));
+        if (e == cudaSuccess)
+            e = cudaMemcpy(g->d_ag_bulk, ab.data(), ab.size() * sizeof(tide::AgSeg), cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess) e = cudaMalloc(&g->d_status, sizeof(int));
     if (e == cudaSuccess) e = cudaMemset(g->d_status, 0, sizeof(int));
     // a table holds the R*P gradient pointers + R shard pointers (reduce-scatter) or R + P
@@ -273,7 +282,9 @@ int tide_group_get_ctas(tide_group_t g, int32_t* rs_ctas, int32_t* ag_ctas) {
     std::lock_guard<std::mutex> lock(g->mu);
     *rs_ctas = g->rs_ctas ? g->rs_ctas
                           : (g->rs_variant == TIDE_RS_REGISTER ? default_ctas(g, tide::kRsCtasPerSm) : g->sm_count);
-    *ag_ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgCtasPerSm);
+    *ag_ctas = g->ag_ctas ? g->ag_ctas
+                          : default_ctas(g, g->ag_variant == TIDE_AG_REGISTER ? tide::kAgCtasPerSm
+                                                                              : tide::kAgBulkCtasPerSm);
     return TIDE_OK;
 }
 
@@ -340,10 +351,18 @@ int tide_all_gather(tide_group_t g, const void* const* shards, void* const* para
     int k = 0;
     if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
     void** dev = g->slots[k].dev;
-    const int ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgCtasPerSm);
-    const cudaError_t e = tide::launch_all_gather(
-        g->d_ag, int(g->plan.ag.size()), g->plan.ag_chunks, reinterpret_cast<const uint16_t* const*>(dev),
-        reinterpret_cast<uint16_t* const*>(dev + R), aligned ? 1 : 0, ctas, st);
+    const auto* sp = reinterpret_cast<const uint16_t* const*>(dev);
+    auto* pp = reinterpret_cast<uint16_t* const*>(dev + R);
+    cudaError_t e;
+    if (aligned && g->d_ag_bulk && g->ag_variant != TIDE_AG_REGISTER) {
+        const int ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgBulkCtasPerSm);
+        e = tide::launch_all_gather_bulk(g->d_ag_bulk, int(g->plan.ag_bulk.size()), g->plan.ag_bulk_chunks, sp, pp,
+                                         ctas, g->d_status, g->timeout_ns, st);
+    } else {
+        const int ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgCtasPerSm);
+        e = tide::launch_all_gather(g->d_ag, int(g->plan.ag.size()), g->plan.ag_chunks, sp, pp, aligned ? 1 : 0, ctas,
+                                    st);
+    }
     if (e != cudaSuccess) return cuda_fail(e);
     return finish_slot(g, k, st);
 }
@@ -363,6 +382,7 @@ int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* p
     bool uniform = pitch >= pl.S * 2;
     for (int r = 1; r < R && uniform; ++r) uniform = static_cast<const char*>(shards[r]) == base + int64_t(r) * pitch;
     if (!uniform && (g->flags & TIDE_FLAG_CE_STRICT)) return TIDE_ELAYOUT;
+    if (g->flags & TIDE_FLAG_CE_1D) uniform = false;  // one 1-D copy per (rank, parameter) run
     int rc = check_device(g);
     if (rc != TIDE_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -407,6 +427,13 @@ int tide_group_set_rs_variant(tide_group_t g, int32_t variant) {
     return TIDE_OK;
 }
 
+int tide_group_set_ag_variant(tide_group_t g, int32_t variant) {
+    if (!g || variant < TIDE_AG_AUTO || variant > TIDE_AG_BULK) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    g->ag_variant = variant;
+    return TIDE_OK;
+}
+
 int tide_group_set_wait_timeout(tide_group_t g, uint64_t timeout_ns) {
     if (!g) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);
@@ -430,6 +457,35 @@ int tide_group_device_status(tide_group_t g, int32_t* status) {
     TIDE_CUDA(cudaMemcpy(&v, g->d_status, sizeof(int), cudaMemcpyDeviceToHost));
     if (v) TIDE_CUDA(cudaMemset(g->d_status, 0, sizeof(int)));
     *status = v;
+    return TIDE_OK;
+}
+
+int tide_stage_into_slots(tide_group_t g, const void* const* grads, void* const* slots, int64_t slot_elems,
+                          void** staged, void* stream) {
+    if (!g || !grads || !slots || !staged) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    const tide::Plan& pl = g->plan;
+    const int R = pl.R, P = pl.P;
+    if (slot_elems < pl.U) return TIDE_ERANGE;
+    for (size_t i = 0; i < size_t(R) * P; ++i)
+        if (!grads[i]) return TIDE_EINVAL;
+    for (int r = 0; r < R; ++r)
+        if (!slots[r]) return TIDE_EINVAL;
+    int rc = check_device(g);
+    if (rc != TIDE_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // parameter p of rank r lands at slot_r + (rows_0*L_0 + ... + rows_{p-1}*L_{p-1}) elements:
+    // the unsharded group, packed without padding, 16-byte aligned when every size is a multiple of 8
+    int64_t off = 0;
+    for (int p = 0; p < P; ++p) {
+        const int64_t n = pl.rows[p] * pl.row_len[p];
+        for (int r = 0; r < R; ++r) {
+            char* dst = static_cast<char*>(slots[r]) + off * 2;
+            TIDE_CUDA(cudaMemcpyAsync(dst, grads[size_t(r) * P + p], size_t(n) * 2, cudaMemcpyDeviceToDevice, st));
+            staged[size_t(r) * P + p] = dst;
+        }
+        off += n;
+    }
     return TIDE_OK;
 }
 

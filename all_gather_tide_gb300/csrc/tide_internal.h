@@ -30,6 +30,15 @@ constexpr int kAgUnroll = 4;
 constexpr int64_t kAgChunk = int64_t(kAgThreads) * 8 * kAgUnroll;  // 8192 elements
 constexpr int kAgCtasPerSm = 4;
 
+// Bulk-copy placement geometry: lane 0 of warp 0 drives the bulk copies, warps 1..3 copy the chunks
+// bulk copies cannot carry; one CTA per SM, kAgBulkStages stages of kAgBulkChunk bf16 (48 KB).
+constexpr int kAgBulkThreads = 128;
+constexpr int64_t kAgBulkChunk = 24576;
+constexpr int kAgBulkStages = 4;
+// Default grid of the bulk placement: more CTAs than fit at once (one per SM) measured faster on
+// GB300 (6.85 vs 6.66 TB/s on the Llama-3.1-70B layer): late CTAs even out the tail.
+constexpr int kAgBulkCtasPerSm = 4;
+
 // One (destination rank d, parameter p) piece of the reduce-scatter output.
 struct RsSeg {
     int64_t dst_off;      // o_p: element offset of the piece in shard d
@@ -66,6 +75,8 @@ struct Plan {
     int64_t rs_bulk_chunks = 0;
     std::vector<AgSeg> ag;
     int64_t ag_chunks = 0;
+    std::vector<AgSeg> ag_bulk;  // same runs, chunked for the bulk-copy placement kernel
+    int64_t ag_bulk_chunks = 0;
 };
 
 // Returns 0 or a negative TIDE_* status.
@@ -85,6 +96,10 @@ size_t bulk_smem_bytes(int R);
 cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, int nsegs, int64_t nchunks, const uint16_t* const* grads,
                                        float* const* shards, int R, int P, int allow_vec, int ctas, int* status,
                                        uint64_t timeout_ns, int inject, cudaStream_t stream);
+size_t ag_bulk_smem_bytes();
+cudaError_t launch_all_gather_bulk(const AgSeg* segs, int nsegs, int64_t nchunks, const uint16_t* const* shards,
+                                   uint16_t* const* params, int ctas, int* status, uint64_t timeout_ns,
+                                   cudaStream_t stream);
 cudaError_t launch_all_gather(const AgSeg* segs, int nsegs, int64_t nchunks,
                               const uint16_t* const* shards, uint16_t* const* params,
                               int allow_vec, int ctas, cudaStream_t stream);

@@ -157,6 +157,41 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def bind_to_gpu_numa_node(device: int) -> dict:
+    """Runs this process on the CPUs next to the GPU, so pinned host buffers are allocated (first
+    touch) in the memory attached to them and host<->device copies take the direct link.  Host
+    side only; nothing about the GPU changes."""
+    info = {"bound": False}
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+        q = subprocess.run(["nvidia-smi", "--query-gpu=uuid,pci.bus_id", "--format=csv,noheader"],
+                           capture_output=True, text=True, timeout=30).stdout
+        bus = None
+        for line in q.strip().splitlines():
+            u, b = [x.strip() for x in line.split(",")]
+            if uuid.replace("GPU-", "") in u or len(q.strip().splitlines()) == 1:
+                bus = b
+        if not bus:
+            return info
+        dom, rest = bus.split(":", 1)
+        sysdir = f"/sys/bus/pci/devices/{dom[-4:].lower()}:{rest.lower()}"
+        with open(os.path.join(sysdir, "local_cpulist")) as f:
+            spec = f.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+            info = {"bound": True, "cpus": len(cpus)}
+        with open(os.path.join(sysdir, "numa_node")) as f:
+            info["numa_node"] = int(f.read().strip())
+    except Exception as e:  # no sysfs entry, no nvidia-smi: leave the process as it is
+        info["error"] = type(e).__name__
+    return info
+
+
 # ---- multi-process aggregation (one replica per GPU; no data-path collective) ----------------
 
 
@@ -196,12 +231,15 @@ def run_tide(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
+    numa = bind_to_gpu_numa_node(local_rank)
     g = workload(args)
     S, U = layout(g)
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
     G.set_ctas(args.rs_ctas, args.ag_ctas)
     G.set_rs_variant({"auto": tide.TIDE_RS_AUTO, "register": tide.TIDE_RS_REGISTER,
                       "bulk": tide.TIDE_RS_BULK}[args.rs_variant])
+    G.set_ag_variant({"auto": tide.TIDE_AG_AUTO, "register": tide.TIDE_AG_REGISTER,
+                      "bulk": tide.TIDE_AG_BULK}[args.ag_variant])
     rs_ctas, ag_ctas = G.get_ctas()
     buf = Buffers(g, S, dev)
     stream = torch.cuda.Stream(device=dev)
@@ -246,10 +284,15 @@ def run_tide(args, rank, world, local_rank):
         "reduce_scatter": {"gbs": b_rs / (rs_avg * 1e-3) / 1e9, "ms": rs_avg, "ms_median": statistics.median(rs_ms),
                            "bytes": b_rs, "ctas": rs_ctas},
         "all_gather_sm": {"gbs": b_ag / (ag_avg * 1e-3) / 1e9, "ms": ag_avg, "ms_median": statistics.median(ag_ms),
-                          "bytes": b_ag, "ctas": ag_ctas},
+                          "bytes": b_ag, "ctas": ag_ctas,
+                          "kernel": "all_gather_kernel" if args.ag_variant == "register" else "all_gather_bulk_kernel"},
     }
-    # copy-engine placement, same buffers (outside the step's timed region)
+    # copy-engine placement and the bulk-copy placement, same buffers (outside the step's timed region)
     legs["all_gather_ce"] = time_ce(G, buf, stream, b_ag, max(3, args.steps))
+    G1 = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_CE_1D)
+    legs["all_gather_ce_1d"] = time_ce(G1, buf, stream, b_ag, max(3, args.steps))
+    G1.close()
+    legs["all_gather_register"] = time_ag_variant(G, buf, stream, b_ag, max(3, args.steps), args, "register")
     for leg in legs.values():
         leg["frac_of_peak"] = leg["gbs"] / peak
 
@@ -287,6 +330,8 @@ def run_tide(args, rank, world, local_rank):
                        "algorithmic_bytes": b_rs}
     out["clocks"] = clocks.summary()
 
+    if args.slot_reuse and rank == 0:
+        out["slot_reuse"] = slot_reuse(G, g, buf, S, U, stream)
     if not args.no_stock and rank == 0:
         out["stock_comparator"] = stock_comparator(G, g, buf, S, U, stream, legs)
     if not args.no_interference and rank == 0:
@@ -295,6 +340,7 @@ def run_tide(args, rank, world, local_rank):
         out["probes"] = probes(G, buf, stream, dev, args)
     if not args.no_e2e:
         out["e2e"] = end_to_end(G, g, buf, S, U, dev, args, world)
+        out["e2e"]["host_affinity"] = numa
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(g, dev, reps=args.cpu_reps)
     G.close()
@@ -382,6 +428,60 @@ def stock_comparator(G, g, buf, S, U, stream, legs):
     del packed, out_shards, padded
     torch.cuda.empty_cache()
     return res
+
+
+# ---- Slot-Reuse staging (Fig. 7) ----------------------------------------------------------------
+
+
+def slot_reuse(G, g, buf, S, U, stream):
+    """Slot-Reuse on one GPU: every rank's gradients are copied (copy engines) into a vacated
+    all-gather slot of R*S bf16 elements, after which the gradient tensors could be released; the
+    reduce-scatter then reads the slots.  Reports the staging time, the reduce-scatter from the
+    slots, and the gradient bytes that become free once staging is enqueued."""
+    slots = torch.empty(g.R, g.R * S, dtype=torch.bfloat16, device=buf.shards.device)
+    staged = G.stage_into_slots(buf.grads, list(slots), g.R * S, stream)
+
+    def timed(fn, reps=3):
+        with torch.cuda.stream(stream):
+            fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    stage_ms = timed(lambda: G.stage_into_slots(buf.grads, list(slots), g.R * S, stream))
+    rs_ms = timed(lambda: G.reduce_scatter(staged, buf.shard_list, stream))
+    inplace_ms = timed(lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream))
+    grad_bytes = g.R * U * 2
+    del slots
+    torch.cuda.empty_cache()
+    return {"stage_ms": stage_ms, "stage_gbs": 2 * grad_bytes / (stage_ms * 1e-3) / 1e9,
+            "rs_from_slots_ms": rs_ms, "rs_in_place_ms": inplace_ms,
+            "grad_bytes_released_after_staging": grad_bytes, "slot_bytes": g.R * g.R * S * 2}
+
+
+def time_ag_variant(G, buf, stream, b_ag, iters, args, variant):
+    import all_gather_tide_gb300 as tide
+
+    G.set_ag_variant({"register": tide.TIDE_AG_REGISTER, "bulk": tide.TIDE_AG_BULK}[variant])
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            G.all_gather(buf.ag_list, buf.params, stream)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(iters)]
+        for e in ev:
+            e[0].record(stream)
+            G.all_gather(buf.ag_list, buf.params, stream)
+            e[1].record(stream)
+    torch.cuda.synchronize()
+    ctas = G.get_ctas()[1]
+    G.set_ag_variant({"auto": tide.TIDE_AG_AUTO, "register": tide.TIDE_AG_REGISTER, "bulk": tide.TIDE_AG_BULK}[args.ag_variant])
+    ms = [e[0].elapsed_time(e[1]) for e in ev]
+    avg = statistics.mean(ms)
+    return {"gbs": b_ag / (avg * 1e-3) / 1e9, "ms": avg, "ms_median": statistics.median(ms), "bytes": b_ag,
+            "ctas": ctas, "kernel": {"register": "all_gather_kernel", "bulk": "all_gather_bulk_kernel"}[variant]}
 
 
 # ---- interference harness ----------------------------------------------------------------------
@@ -474,7 +574,7 @@ def cta_sweep(G, buf, stream, args, concurrent):
 
     rows = []
     cases = [("reduce_scatter", v, n) for v in (tide.TIDE_RS_REGISTER, tide.TIDE_RS_BULK) for n in args.sweep_rs]
-    cases += [("all_gather_sm", 0, n) for n in args.sweep_ag]
+    cases += [("all_gather_sm", v, n) for v in (tide.TIDE_AG_REGISTER, tide.TIDE_AG_BULK) for n in args.sweep_ag]
     for kind, variant, n in cases:
         if kind == "reduce_scatter":
             G.set_ctas(n, 0)
@@ -483,6 +583,7 @@ def cta_sweep(G, buf, stream, args, concurrent):
             nbytes, reps = g_rs, 1
         else:
             G.set_ctas(0, n)
+            G.set_ag_variant(variant)
             launch = lambda: [G.all_gather(buf.ag_list, buf.params, stream) for _ in range(8)]
             nbytes, reps = g_ag * 8, 8
         with torch.cuda.stream(stream):
@@ -494,11 +595,12 @@ def cta_sweep(G, buf, stream, args, concurrent):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
         c = concurrent(launch, kind, reps=2)
-        rows.append({"kind": kind, "variant": {0: "-", 1: "register", 2: "bulk"}[variant], "ctas": n,
+        rows.append({"kind": kind, "variant": {0: "auto", 1: "register", 2: "bulk"}[variant], "ctas": n,
                      "alone_ms": ms / reps, "gbs": nbytes / (ms * 1e-3) / 1e9,
                      "gemm_slowdown_pct": c["slowdown_pct"], "gemms": c["gemms_started_inside"]})
     G.set_ctas(args.rs_ctas, args.ag_ctas)
     G.set_rs_variant(tide.TIDE_RS_AUTO)
+    G.set_ag_variant(tide.TIDE_AG_AUTO)
     return rows
 
 
@@ -817,6 +919,7 @@ def main():
     ap.add_argument("--rs-ctas", type=int, default=0)
     ap.add_argument("--ag-ctas", type=int, default=0)
     ap.add_argument("--rs-variant", choices=["auto", "register", "bulk"], default="auto")
+    ap.add_argument("--ag-variant", choices=["auto", "register", "bulk"], default="auto")
     ap.add_argument("--interference-ctas", type=int, nargs="*", default=[16, 32])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-reps", type=int, default=4)
@@ -824,6 +927,7 @@ def main():
     ap.add_argument("--sweep-rs", type=int, nargs="*", default=[8, 16, 20, 24, 32, 48, 64, 96, 152, 304])
     ap.add_argument("--sweep-ag", type=int, nargs="*", default=[8, 16, 24, 32, 64, 152, 608])
     ap.add_argument("--probes", action="store_true", help="spin-CTA curve, SM-id probe and Table 4 victims")
+    ap.add_argument("--slot-reuse", action="store_true", help="Slot-Reuse staging leg")
     ap.add_argument("--spin-ctas", type=int, nargs="*", default=[1, 4, 8, 12, 16, 20, 24, 32, 48, 64, 96, 152])
     ap.add_argument("--no-interference", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -60,6 +60,9 @@ extern "C" {
 /* Return TIDE_ELAYOUT from tide_all_gather_ce instead of falling back to one 1-D copy per
  * (rank, parameter) when shards[r] != shards[0] + r*pitch for one pitch >= S*2 bytes. */
 #define TIDE_FLAG_CE_STRICT 0x2u
+/* tide_all_gather_ce issues one 1-D cudaMemcpyAsync per (rank, parameter) run of valid rows instead
+ * of one 2-D copy per parameter (R*P copies instead of about P). */
+#define TIDE_FLAG_CE_1D 0x4u
 
 typedef struct tide_group *tide_group_t;
 
@@ -98,8 +101,9 @@ int tide_group_valid_rows(tide_group_t g, int32_t d, int32_t p, int64_t *v);
 
 /*
  * CTA counts of the reduce-scatter and all-gather kernels.  0 restores the default (enough
- * CTAs to fill every SM: one per SM for the bulk-copy reduce-scatter, two for the register path,
- * four for the placement); a positive value is used as given (at most the work's chunk count),
+ * CTAs to fill every SM: one per SM for the bulk-copy reduce-scatter, two for its register path,
+ * four per SM for either placement kernel); a positive value is used as given (at most the work's
+ * chunk count),
  * so a caller can leave SMs to concurrent compute (Fig. 3, Fig. 4, Table 4).
  */
 int tide_group_set_ctas(tide_group_t g, int32_t rs_ctas, int32_t ag_ctas);
@@ -158,15 +162,24 @@ int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *p
  */
 int tide_group_set_rs_variant(tide_group_t g, int32_t variant);
 
+#define TIDE_AG_AUTO 0     /* bulk-copy placement when every pointer is 16-byte aligned, else register path */
+#define TIDE_AG_REGISTER 1 /* 16-byte register loads and stores, 4 CTAs per SM */
+#define TIDE_AG_BULK 2     /* 48 KB bulk copies in and out of shared memory driven by one thread per CTA */
+
+/* Chooses the placement kernel of tide_all_gather; both write the same bits.  The bulk path needs
+ * 16-byte aligned pointers; otherwise the register path runs. */
+int tide_group_set_ag_variant(tide_group_t g, int32_t variant);
+
 /*
- * Every device-side wait of the library's kernels (the bulk path's mbarrier waits) gives up after
+ * Every device-side wait of the library's kernels (the bulk paths' mbarrier waits) gives up after
  * `timeout_ns` (0 = the default, 2 s): it writes a nonzero code to the group's device status word,
  * the CTA drains its own copies in flight and returns.  Nothing traps.
  */
 int tide_group_set_wait_timeout(tide_group_t g, uint64_t timeout_ns);
 
-/* Reads the group's device status word (0 = no wait expired; 1 = a consumer wait expired,
- * 2 = a producer wait expired, 4 = draining copies after an abort expired) and clears it.
+/* Reads the group's device status word (0 = no wait expired; 1 = a reduce-scatter consumer wait
+ * expired, 2 = a reduce-scatter producer wait expired, 4 = draining copies after an abort expired,
+ * 8 = a placement load wait expired) and clears it.
  * Synchronous: copies from the device. */
 int tide_group_device_status(tide_group_t g, int32_t *status);
 
@@ -174,6 +187,22 @@ int tide_group_device_status(tide_group_t g, int32_t *status);
  * the consumers' bounded waits expire and the status word reports it (no copy is issued). */
 #define TIDE_DEBUG_STALL_PRODUCER 0x1u
 int tide_group_set_debug(tide_group_t g, uint32_t flags);
+
+/*
+ * tide_stage_into_slots — Slot-Reuse staging (abstract: "Slot-Reuse optionally stages gradients
+ * in vacated all-gather slots"; Fig. 7: the gradients are copied into a vacated all-gather slot and
+ * the slot's reuse is gated on read completion).  For every rank r it copies the P gradients of
+ * grads[r*P + p] with copy engines (one cudaMemcpyAsync each, stream-ordered) into slots[r], packed
+ * in parameter order without padding (parameter p at element rows_0*L_0 + ... + rows_{p-1}*L_{p-1}),
+ * and writes the staged addresses to staged[r*P + p] (host array of R*P pointers).  Once the copies
+ * are enqueued the caller may release the gradient tensors for reuse after the stream reaches them;
+ * tide_reduce_scatter(g, staged, shards, stream) then reads the slots, and the caller gates the
+ * slots' next use on an event recorded after it.
+ *   slot_elems: bf16 elements available in each slot (the all-gather output of the group holds
+ *   R*S >= U); TIDE_ERANGE if slot_elems < U.
+ */
+int tide_stage_into_slots(tide_group_t g, const void *const *grads, void *const *slots, int64_t slot_elems,
+                          void **staged, void *stream);
 
 /* Copies issued by the last tide_all_gather_ce on g, and whether the uniform-pitch form was used. */
 int tide_group_last_ce_copies(tide_group_t g, int64_t *copies, int32_t *uniform_pitch);

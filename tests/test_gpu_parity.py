@@ -112,7 +112,7 @@ def run_rs(tide, g, ctas=0, misalign=False, flags=0, variant=0):
     G.close()
 
 
-def run_ag(tide, g, ce=False, ctas=0, misalign=False, uniform=True, flags=0):
+def run_ag(tide, g, ce=False, ctas=0, misalign=False, uniform=True, flags=0, variant=0):
     lay = oracle.plan(g.R, g.rows, g.row_len)
     host = []
     for r in range(g.R):
@@ -139,11 +139,13 @@ def run_ag(tide, g, ce=False, ctas=0, misalign=False, uniform=True, flags=0):
     params = [Guarded(g.numel(p), torch.int16, fill=BF16_SENTINEL, offset_elems=off) for p in range(g.P)]
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
     G.set_ctas(0, ctas)
+    G.set_ag_variant(variant)
     if ce:
         G.all_gather_ce(shard_views, [x.view for x in params])
     else:
         G.all_gather(shard_views, [x.view for x in params])
     torch.cuda.synchronize()
+    assert G.device_status() == 0
     for p in range(g.P):
         got = params[p].view.cpu().numpy().view(np.uint16)
         bad = np.nonzero(got != want[p])[0]
@@ -254,7 +256,24 @@ def test_bulk_wait_timeout_reports_status_and_context_survives(tide):
 
 @pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
 def test_all_gather_matches_oracle(tide, g):
-    run_ag(tide, g)
+    run_ag(tide, g)  # default: bulk-copy placement for aligned pointers
+
+
+@pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
+def test_all_gather_register_matches_oracle(tide, g):
+    run_ag(tide, g, variant=tide.TIDE_AG_REGISTER)
+
+
+@pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
+def test_all_gather_bulk_matches_oracle(tide, g):
+    run_ag(tide, g, variant=tide.TIDE_AG_BULK)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 16, 152])
+def test_all_gather_bulk_cta_counts(tide, ctas):
+    run_ag(tide, group("qwen3moe").scaled(16), ctas=ctas, variant=tide.TIDE_AG_BULK)
+    run_ag(tide, group("llama70b").scaled(16), ctas=ctas, variant=tide.TIDE_AG_BULK)
+    run_ag(tide, group("qwen3moe").scaled(16), ctas=ctas, variant=tide.TIDE_AG_BULK, misalign=True)
 
 
 @pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
@@ -277,6 +296,14 @@ def test_misaligned_pointers_take_elementwise_path(tide):
     run_rs(tide, g, misalign=True)
     run_ag(tide, g, misalign=True)
     run_ag(tide, g, misalign=True, ce=True)
+
+
+def test_ce_one_dimensional_mode(tide):
+    g = group("qwen3moe").scaled(16)
+    copies, uniform = run_ag(tide, g, ce=True, flags=tide.TIDE_FLAG_CE_1D)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    assert not uniform
+    assert copies == sum(1 for r in range(g.R) for p in range(g.P) if lay.valid_rows(r, p) > 0)
 
 
 def test_vec_strict_rejects_misaligned(tide):
@@ -420,10 +447,13 @@ def test_full_size_all_gather(tide, name):
     lay = oracle.plan(g.R, g.rows, g.row_len)
     shards = torch.stack([rng.shard_bits(g, r, lay.S, device="cuda") for r in range(g.R)])
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
-    for ce in (False, True):
+    for mode in ("register", "ce", "bulk"):
+        ce = mode == "ce"
+        G.set_ag_variant(tide.TIDE_AG_BULK if mode == "bulk" else tide.TIDE_AG_REGISTER)
         params = [torch.full((g.numel(p),), BF16_SENTINEL, dtype=torch.int16, device="cuda") for p in range(g.P)]
         (G.all_gather_ce if ce else G.all_gather)(list(shards), params)
         torch.cuda.synchronize()
+        assert G.device_status() == 0
         rs = np.random.default_rng(7)
         for p in range(g.P):
             n = g.numel(p)
@@ -435,12 +465,44 @@ def test_full_size_all_gather(tide, name):
                 want[sel] = rng.shard_bits(g, int(a), 0, idx=torch.from_numpy(jj[sel])).numpy().astype(np.int64)
             want &= 0xFFFF
             got = params[p][torch.from_numpy(idx).cuda()].cpu().numpy().astype(np.int64) & 0xFFFF
-            assert np.array_equal(got, want), (ce, p)
+            assert np.array_equal(got, want), (mode, p)
             for rr in range(g.R):
                 v = lay.valid_rows(rr, p) * int(lay.row_len[p])
                 s, o = int(lay.s[p]), int(lay.o[p])
-                assert torch.equal(params[p][rr * s: rr * s + v], shards[rr, o:o + v]), (ce, p, rr)
+                assert torch.equal(params[p][rr * s: rr * s + v], shards[rr, o:o + v]), (mode, p, rr)
         del params
     G.close()
     del shards
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("g", [group("tiny"), group("llama70b").scaled(32), group("qwen3moe").scaled(16),
+                               group("wan_r64").scaled(16)], ids=lambda g: g.name)
+def test_slot_reuse_staging(tide, g):
+    """Gradients staged into all-gather-sized slots, the originals overwritten right after (as if
+    released), then the reduce-scatter from the slots: the oracle's result, bit for bit."""
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    host = rng.group_grads(g)
+    want = np.stack(oracle.reduce_scatter(lay, [[t.numpy().view(np.uint16) for t in row] for row in host]))
+    grads = [[t.cuda() for t in row] for row in host]
+    slot_elems = g.R * lay.S
+    slots = torch.full((g.R, slot_elems), BF16_SENTINEL, dtype=torch.int16, device="cuda")
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+    staged = G.stage_into_slots(grads, list(slots), slot_elems)
+    for row in grads:  # released: later work reuses the memory (here: overwritten with NaN bits)
+        for t in row:
+            t.fill_(0x7FC0)
+    out = torch.empty(g.R, lay.S, dtype=torch.float32, device="cuda")
+    G.reduce_scatter(staged, list(out))
+    torch.cuda.synchronize()
+    assert np.array_equal(f32_bits(out), want.view(np.uint32))
+    # the slots hold each rank's unsharded gradients packed in parameter order
+    flat = slots.cpu().numpy().view(np.uint16)
+    for r in range(g.R):
+        packed = np.concatenate([host[r][p].numpy().view(np.uint16) for p in range(g.P)])
+        assert np.array_equal(flat[r, :packed.size], packed)
+        assert np.all(flat[r, packed.size:] == (BF16_SENTINEL & 0xFFFF))
+    with pytest.raises(tide.TideError) as e:
+        G.stage_into_slots(grads, list(slots), lay.U - 1)
+    assert e.value.status == tide.TIDE_ERANGE
+    G.close()
