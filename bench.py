@@ -240,6 +240,8 @@ def run_tide(args, rank, world, local_rank):
                       "bulk": tide.TIDE_RS_BULK}[args.rs_variant])
     G.set_ag_variant({"auto": tide.TIDE_AG_AUTO, "register": tide.TIDE_AG_REGISTER,
                       "bulk": tide.TIDE_AG_BULK}[args.ag_variant])
+    if args.ce_lanes:
+        G.set_ce_lanes(args.ce_lanes)
     rs_ctas, ag_ctas = G.get_ctas()
     buf = Buffers(g, S, dev)
     stream = torch.cuda.Stream(device=dev)
@@ -289,8 +291,16 @@ def run_tide(args, rank, world, local_rank):
     }
     # copy-engine placement and the bulk-copy placement, same buffers (outside the step's timed region)
     legs["all_gather_ce"] = time_ce(G, buf, stream, b_ag, max(3, args.steps))
-    G1 = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_CE_1D)
-    legs["all_gather_ce_1d"] = time_ce(G1, buf, stream, b_ag, max(3, args.steps))
+    G1 = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_CE_2D)
+    if args.ce_lanes:
+        G1.set_ce_lanes(args.ce_lanes)
+    legs["all_gather_ce_2d"] = time_ce(G1, buf, stream, b_ag, max(3, args.steps))
+    for lanes in args.ce_lanes_sweep:
+        for name, grp in (("1d", G), ("2d", G1)):
+            grp.set_ce_lanes(lanes)
+            legs[f"all_gather_ce_{name}_lanes{lanes}"] = time_ce(grp, buf, stream, b_ag, max(3, args.steps))
+    if args.ce_lanes_sweep:
+        G.set_ce_lanes(args.ce_lanes or 8)
     G1.close()
     legs["all_gather_register"] = time_ag_variant(G, buf, stream, b_ag, max(3, args.steps), args, "register")
     for leg in legs.values():
@@ -920,6 +930,8 @@ def main():
     ap.add_argument("--ag-ctas", type=int, default=0)
     ap.add_argument("--rs-variant", choices=["auto", "register", "bulk"], default="auto")
     ap.add_argument("--ag-variant", choices=["auto", "register", "bulk"], default="auto")
+    ap.add_argument("--ce-lanes", type=int, default=0, help="copy-engine streams (0 = library default)")
+    ap.add_argument("--ce-lanes-sweep", type=int, nargs="*", default=[])
     ap.add_argument("--interference-ctas", type=int, nargs="*", default=[16, 32])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-reps", type=int, default=4)

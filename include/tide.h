@@ -57,12 +57,12 @@ extern "C" {
 /* Return TIDE_EALIGN instead of running the element-wise path when a pointer passed to
  * tide_reduce_scatter / tide_all_gather is not 16-byte aligned. */
 #define TIDE_FLAG_VEC_STRICT 0x1u
-/* Return TIDE_ELAYOUT from tide_all_gather_ce instead of falling back to one 1-D copy per
- * (rank, parameter) when shards[r] != shards[0] + r*pitch for one pitch >= S*2 bytes. */
+/* With TIDE_FLAG_CE_2D: return TIDE_ELAYOUT from tide_all_gather_ce instead of falling back to
+ * 1-D copies when shards[r] != shards[0] + r*pitch for one pitch >= S*2 bytes. */
 #define TIDE_FLAG_CE_STRICT 0x2u
-/* tide_all_gather_ce issues one 1-D cudaMemcpyAsync per (rank, parameter) run of valid rows instead
- * of one 2-D copy per parameter (R*P copies instead of about P). */
-#define TIDE_FLAG_CE_1D 0x4u
+/* tide_all_gather_ce issues one 2-D copy per parameter (the paper's form, about P copies) instead
+ * of the default one 1-D copy per (rank, parameter) run of valid rows (R*P copies). */
+#define TIDE_FLAG_CE_2D 0x4u
 
 typedef struct tide_group *tide_group_t;
 
@@ -140,12 +140,14 @@ int tide_all_gather(tide_group_t g, const void *const *shards, void *const *para
                     void *stream);
 
 /*
- * tide_all_gather_ce — the same placement with copy engines and no SM kernel (Fig. 5b: one
- * strided copy per parameter; Table 1 "AG SM budget 0").  When shards[r] = shards[0] + r*pitch
- * for one pitch >= S*2 bytes, each parameter takes one cudaMemcpy2DAsync over its full ranks
- * (height f_p = floor(rows_p/m_p), width s_p*2 bytes) plus at most one cudaMemcpyAsync for the
- * rank holding its last partial piece.  Otherwise it falls back to one cudaMemcpyAsync per
- * (rank, parameter) with valid rows (or returns TIDE_ELAYOUT under TIDE_FLAG_CE_STRICT).
+ * tide_all_gather_ce — the same placement with copy engines and no SM kernel (Table 1 "AG SM
+ * budget 0"; Fig. 5b).  By default one cudaMemcpyAsync per (rank, parameter) run of valid rows,
+ * spread over the group's copy-engine lanes (tide_group_set_ce_lanes; default 8): measured on
+ * GB300 this is the fast form.  With TIDE_FLAG_CE_2D, and when shards[r] = shards[0] + r*pitch for
+ * one pitch >= S*2 bytes, each parameter instead takes the paper's one strided copy: one
+ * cudaMemcpy2DAsync over its full ranks (height f_p = floor(rows_p/m_p), width s_p*2 bytes) plus at
+ * most one cudaMemcpyAsync for the rank holding its last partial piece; without a uniform pitch it
+ * falls back to the 1-D copies (or returns TIDE_ELAYOUT under TIDE_FLAG_CE_STRICT).
  */
 int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *params,
                        void *stream);
@@ -203,6 +205,15 @@ int tide_group_set_debug(tide_group_t g, uint32_t flags);
  */
 int tide_stage_into_slots(tide_group_t g, const void *const *grads, void *const *slots, int64_t slot_elems,
                           void **staged, void *stream);
+
+/*
+ * Spreads the copy-engine work of tide_all_gather_ce and tide_stage_into_slots over `lanes`
+ * (1..8, default 8) streams: the copies start after the work already enqueued on the caller's stream, and the
+ * caller's stream waits for all of them, so the calls stay stream-ordered.  Several streams keep
+ * several copy engines busy at once.  The helper streams are created on first use and destroyed
+ * with the group.
+ */
+int tide_group_set_ce_lanes(tide_group_t g, int32_t lanes);
 
 /* Copies issued by the last tide_all_gather_ce on g, and whether the uniform-pitch form was used. */
 int tide_group_last_ce_copies(tide_group_t g, int64_t *copies, int32_t *uniform_pitch);

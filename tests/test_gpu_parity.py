@@ -278,7 +278,17 @@ def test_all_gather_bulk_cta_counts(tide, ctas):
 
 @pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
 def test_all_gather_ce_matches_oracle(tide, g):
+    """Default copy-engine form: one 1-D copy per (rank, parameter) run of valid rows."""
     copies, uniform = run_ag(tide, g, ce=True)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    assert not uniform
+    assert copies == sum(1 for r in range(g.R) for p in range(g.P) if lay.valid_rows(r, p) > 0)
+
+
+@pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
+def test_all_gather_ce_2d_matches_oracle(tide, g):
+    """The paper's form: one strided (2-D) copy per parameter over its full ranks."""
+    copies, uniform = run_ag(tide, g, ce=True, flags=tide.TIDE_FLAG_CE_2D)
     assert uniform
     lay = oracle.plan(g.R, g.rows, g.row_len)
     expect = sum((r // int(m) > 0) + (r % int(m) > 0) for r, m in zip(g.rows, lay.m))
@@ -298,14 +308,6 @@ def test_misaligned_pointers_take_elementwise_path(tide):
     run_ag(tide, g, misalign=True, ce=True)
 
 
-def test_ce_one_dimensional_mode(tide):
-    g = group("qwen3moe").scaled(16)
-    copies, uniform = run_ag(tide, g, ce=True, flags=tide.TIDE_FLAG_CE_1D)
-    lay = oracle.plan(g.R, g.rows, g.row_len)
-    assert not uniform
-    assert copies == sum(1 for r in range(g.R) for p in range(g.P) if lay.valid_rows(r, p) > 0)
-
-
 def test_vec_strict_rejects_misaligned(tide):
     g = group("tiny")
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_VEC_STRICT)
@@ -319,7 +321,7 @@ def test_vec_strict_rejects_misaligned(tide):
 
 def test_ce_non_uniform_pitch_falls_back(tide):
     g = group("qwen3moe").scaled(16)
-    copies, uniform = run_ag(tide, g, ce=True, uniform=False)
+    copies, uniform = run_ag(tide, g, ce=True, uniform=False, flags=tide.TIDE_FLAG_CE_2D)
     assert not uniform
     lay = oracle.plan(g.R, g.rows, g.row_len)
     assert copies == sum(1 for r in range(g.R) for p in range(g.P) if lay.valid_rows(r, p) > 0)
@@ -327,7 +329,7 @@ def test_ce_non_uniform_pitch_falls_back(tide):
 
 def test_ce_strict_rejects_non_uniform_pitch(tide):
     g = group("tiny")
-    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_CE_STRICT)
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_CE_STRICT | tide.TIDE_FLAG_CE_2D)
     buf = torch.zeros(16 * G.S, dtype=torch.bfloat16, device="cuda")
     shards = [buf[a:a + G.S] for a in (0, 2 * G.S, 3 * G.S, 6 * G.S)]  # pitches 2S, S, 3S
     params = [torch.zeros(g.numel(p), dtype=torch.bfloat16, device="cuda") for p in range(g.P)]
@@ -505,4 +507,33 @@ def test_slot_reuse_staging(tide, g):
     with pytest.raises(tide.TideError) as e:
         G.stage_into_slots(grads, list(slots), lay.U - 1)
     assert e.value.status == tide.TIDE_ERANGE
+    G.close()
+
+
+@pytest.mark.parametrize("lanes", [1, 2, 4, 8])
+@pytest.mark.parametrize("flags", [0, 4], ids=["1d", "2d"])
+def test_ce_lanes_stay_stream_ordered(tide, lanes, flags):
+    """Copy-engine placement spread over helper streams: it sees work enqueued just before it on the
+    caller's stream and the caller's stream sees its result right after, with no host sync."""
+    g = group("qwen3moe").scaled(8)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    src = torch.stack([rng.shard_bits(g, r, lay.S) for r in range(g.R)]).cuda()
+    want = oracle.all_gather(lay, [a.cpu().numpy().view(np.uint16) for a in src],
+                             [np.zeros(g.numel(p), np.uint16) for p in range(g.P)])
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
+    G.set_ce_lanes(lanes)
+    st = torch.cuda.Stream()
+    shards = torch.zeros_like(src)
+    params = [torch.zeros(g.numel(p), dtype=torch.int16, device="cuda") for p in range(g.P)]
+    outs = [torch.empty_like(x) for x in params]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        torch.cuda._sleep(2_000_000)  # keep the stream busy so ordering, not luck, decides
+        shards.copy_(src)
+        G.all_gather_ce(list(shards), params, st)
+        for o, x in zip(outs, params):
+            o.copy_(x)
+    torch.cuda.synchronize()
+    for p in range(g.P):
+        assert np.array_equal(outs[p].cpu().numpy().view(np.uint16), want[p]), (lanes, p)
     G.close()
