@@ -28,6 +28,10 @@ import threading
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
+# The harness runs a collective (up to 8 copy-engine streams) beside a victim on its own stream; with
+# the default 8 hardware work queues, streams would share queues and the victim would wait behind
+# copies instead of running beside them.  Set before CUDA starts (importing torch does not start it).
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
 sys.path.insert(0, ROOT)
 
 import numpy as np  # noqa: E402
@@ -527,6 +531,7 @@ def interference(G, buf, stream, dev, args):
         starts while the collective runs, and its time includes any wait for free SMs."""
         inside = []
         coll_ms = []
+        done_inside, window = [0], [0.0]
         for _ in range(reps):
             torch.cuda.synchronize()
             s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -548,7 +553,14 @@ def interference(G, buf, stream, dev, args):
             for e in ge:
                 if 0 <= s0.elapsed_time(e[0]) < end:
                     inside.append(e[0].elapsed_time(e[1]))
-        res = {"collective_ms": statistics.median(coll_ms), "gemms_started_inside": len(inside)}
+                if s0.elapsed_time(e[1]) <= end:
+                    done_inside[0] += 1
+            # the rate is taken over the part of the window in which GEMMs were queued
+            window[0] += min(end, s0.elapsed_time(ge[-1][1]))
+        res = {"collective_ms": statistics.median(coll_ms), "gemms_started_inside": len(inside),
+               # GEMM work finished inside the collective's window, as a fraction of what the GEMM
+               # alone would finish in that time (1.0 = unaffected; also captures GEMMs kept waiting)
+               "victim_rate": done_inside[0] * t_alone / window[0] if window[0] else None}
         if inside:
             res["gemm_ms"] = statistics.median(inside)
             res["slowdown_pct"] = 100.0 * (statistics.median(inside) / t_alone - 1.0)

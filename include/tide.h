@@ -211,7 +211,9 @@ int tide_stage_into_slots(tide_group_t g, const void *const *grads, void *const 
  * (1..8, default 8) streams: the copies start after the work already enqueued on the caller's stream, and the
  * caller's stream waits for all of them, so the calls stay stream-ordered.  Several streams keep
  * several copy engines busy at once.  The helper streams are created on first use and destroyed
- * with the group.
+ * with the group.  CUDA maps streams onto CUDA_DEVICE_MAX_CONNECTIONS hardware queues (8 by
+ * default); when the lanes plus the application's other busy streams exceed that, unrelated work
+ * can queue behind the copies, so raise it (up to 32) before CUDA starts or use fewer lanes.
  */
 int tide_group_set_ce_lanes(tide_group_t g, int32_t lanes);
 
