@@ -10,7 +10,7 @@
 // size of each copy (measured on GB300: about 17 GB/s per SM with 4 KB copies, about 185 GB/s per
 // SM with 48 KB copies).  The kernel therefore streams one rank's row of a chunk per copy: a chunk
 // is kBulkChunk elements of one (destination, parameter) piece, and its R rows pass through
-// kBulkStages shared-memory stages of kBulkChunk bf16 elements, rank 0 first.  The fp32 sums of
+// up to kBulkMaxStages shared-memory stages of kBulkChunk bf16 elements, rank 0 first.  The fp32 sums of
 // the chunk stay in the consumers' registers across the R stages (ascending rank order, starting
 // from rank 0's value, exact bf16 -> fp32 widening, __fadd_rn), and are stored once, straight to
 // the destination shard (st.global.cs), after the last rank.
@@ -236,21 +236,21 @@ __device__ __forceinline__ void st_cs_v8(float* p, const float (&a)[8]) {
 __global__ void __launch_bounds__(kBulkThreads, 1)
 reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nchunks,
                            const uint16_t* const* __restrict__ grads, float* const* __restrict__ shards, int R,
-                           int P, int allow_vec, int* status, uint64_t timeout_ns, int inject) {
+                           int P, int allow_vec, int stages, int* status, uint64_t timeout_ns, int inject) {
     constexpr int kConsumers = kBulkConsumerWarps * 32;
     constexpr int kGroups = int(kBulkChunk / 8 / kConsumers);  // 8-element groups per consumer thread
     static_assert(kBulkChunk % (8 * kConsumers) == 0, "chunk must split evenly over the consumers");
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-    uint64_t* empty = full + kBulkStages;
+    uint64_t* empty = full + kBulkMaxStages;
     unsigned char* data = smem + 128;  // stage s at data + s * kBulkChunk * 2
     // the R gradient pointers of the producer's current piece
-    const uint16_t** gptr = reinterpret_cast<const uint16_t**>(data + int64_t(kBulkStages) * kBulkChunk * 2);
+    const uint16_t** gptr = reinterpret_cast<const uint16_t**>(data + int64_t(stages) * kBulkChunk * 2);
     __shared__ int abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kBulkStages; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kBulkConsumerWarps);
         }
@@ -263,7 +263,9 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nc
     if (warp == kBulkConsumerWarps) {
         // ---------------- producer warp: all lanes track the piece, lane 0 issues ----------------
         PieceCursor pc;
-        int64_t it = 0;  // stage uses issued so far (lane 0)
+        int64_t it = 0;       // stage uses issued so far (lane 0)
+        int s = 0;            // stage of use `it`
+        uint32_t phase = 0;   // its phase parity
         for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
             if (pc.seek(segs, nsegs, c)) {
                 for (int r = lane; r < R; r += 32) gptr[r] = grads[int64_t(r) * P + pc.p];
@@ -274,28 +276,32 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nc
             int stop = 0;
             if (lane == 0) {
                 const uint32_t bytes = uint32_t(v.nbulk * 2);
-                for (int r = 0; r < R; ++r, ++it) {
-                    const int s = int(it % kBulkStages);
-                    const uint32_t phase = uint32_t((it / kBulkStages) & 1);
+                for (int r = 0; r < R; ++r) {
                     if (!wait_bounded(&empty[s], phase ^ 1u, timeout_ns, abort, status, 2)) {
                         stop = 1;
                         break;
                     }
-                    if (inject) continue;  // test hook: never signal the stage
-                    mbar_arrive_expect_tx(&full[s], bytes);
-                    bulk_g2s(data + int64_t(s) * kBulkChunk * 2, gptr[r] + v.src, bytes, &full[s]);
+                    if (!inject) {  // test hook: never signal the stage
+                        mbar_arrive_expect_tx(&full[s], bytes);
+                        bulk_g2s(data + int64_t(s) * kBulkChunk * 2, gptr[r] + v.src, bytes, &full[s]);
+                    }
+                    ++it;
+                    if (++s == stages) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
                 }
             }
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
         }
         // On abort, let the copies already issued land before the CTA's shared memory goes away.
-        // Only the last kBulkStages stage uses can still be in flight, and each is the newest phase
+        // Only the last `stages` stage uses can still be in flight, and each is the newest phase
         // of its stage, so waiting for that phase's parity is exact.
         if (lane == 0 && *abort && !inject) {
             const uint64_t drain = globaltimer() + 100000000ull;  // at most 100 ms
-            for (int64_t j = max(int64_t(0), it - kBulkStages); j < it; ++j) {
-                uint64_t* bar = &full[j % kBulkStages];
-                const uint32_t par = uint32_t((j / kBulkStages) & 1);
+            for (int64_t j = max(int64_t(0), it - stages); j < it; ++j) {
+                uint64_t* bar = &full[j % stages];
+                const uint32_t par = uint32_t((j / stages) & 1);
                 while (!mbar_try_wait(bar, par)) {
                     if (globaltimer() > drain) {
                         atomicCAS(status, 0, 4);
@@ -311,7 +317,8 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nc
     const int ctid = threadIdx.x;
     PieceCursor pc;
     float* shard = nullptr;
-    int64_t it = 0;
+    int s = 0;
+    uint32_t phase = 0;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
         if (pc.seek(segs, nsegs, c)) shard = shards[pc.d];
         const ChunkView v = pc.view(c, kBulkChunk, allow_vec);
@@ -319,15 +326,17 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nc
         if (v.nbulk > 0) {
             const bool whole = v.nbulk == kBulkChunk;  // every group of the chunk is carried
             float acc[kGroups][8];
-            for (int r = 0; r < R; ++r, ++it) {
-                const int s = int(it % kBulkStages);
-                const uint32_t phase = uint32_t((it / kBulkStages) & 1);
+            for (int r = 0; r < R; ++r) {
                 if (!wait_bounded(&full[s], phase, timeout_ns, abort, status, 1)) return;
                 const uint4* row = reinterpret_cast<const uint4*>(data + int64_t(s) * kBulkChunk * 2);
                 if (r == 0) accumulate_row<true, kGroups, kConsumers>(acc, row, ctid, whole, v.nbulk);
                 else accumulate_row<false, kGroups, kConsumers>(acc, row, ctid, whole, v.nbulk);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
+                if (++s == stages) {
+                    s = 0;
+                    phase ^= 1u;
+                }
             }
             const bool wide = (reinterpret_cast<uintptr_t>(dst) & 31u) == 0;  // 32-byte stores possible
 #pragma unroll
@@ -351,19 +360,30 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nc
 
 }  // namespace
 
-size_t bulk_smem_bytes(int R) { return 128 + size_t(kBulkStages) * size_t(kBulkChunk) * 2 + sizeof(void*) * size_t(R); }
+size_t bulk_smem_bytes(int R, int stages) {
+    return 128 + size_t(stages) * size_t(kBulkChunk) * 2 + sizeof(void*) * size_t(R);
+}
+
+// The deepest pipeline whose stages and pointer cache fit in one CTA's shared memory.
+int bulk_stages(int R) {
+    for (int st = kBulkMaxStages; st >= 2; --st)
+        if (bulk_smem_bytes(R, st) <= kMaxDynamicSmem) return st;
+    return 0;
+}
 
 cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, int nsegs, int64_t nchunks, const uint16_t* const* grads,
                                        float* const* shards, int R, int P, int allow_vec, int ctas, int* status,
                                        uint64_t timeout_ns, int inject, cudaStream_t stream) {
     if (nchunks <= 0) return cudaSuccess;
-    const size_t smem = bulk_smem_bytes(R);
+    const int stages = bulk_stages(R);
+    if (stages < 2) return cudaErrorInvalidValue;
+    const size_t smem = bulk_smem_bytes(R, stages);
     cudaError_t e = cudaFuncSetAttribute(reduce_scatter_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
     const int grid = int(std::min<int64_t>(ctas, nchunks));
     reduce_scatter_bulk_kernel<<<grid, kBulkThreads, smem, stream>>>(segs, nsegs, nchunks, grads, shards, R, P,
-                                                                     allow_vec, status, timeout_ns, inject);
+                                                                     allow_vec, stages, status, timeout_ns, inject);
     return cudaGetLastError();
 }
 

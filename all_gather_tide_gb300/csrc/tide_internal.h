@@ -16,12 +16,13 @@ constexpr int64_t kRsChunk = int64_t(kRsThreads) * 8 * kRsUnroll;  // 4096 eleme
 constexpr int kRsCtasPerSm = 2;
 
 // Bulk-copy reduce-scatter geometry: 1 producer warp + kBulkConsumerWarps consumer warps, one CTA
-// per SM (16 warps in all), kBulkStages shared-memory stages of one rank row of a kBulkChunk-element
+// per SM (16 warps in all), up to kBulkMaxStages shared-memory stages of one rank row of a kBulkChunk-element
 // chunk (45 KB).
 constexpr int kBulkConsumerWarps = 15;
 constexpr int kBulkThreads = (kBulkConsumerWarps + 1) * 32;
 constexpr int64_t kBulkChunk = 23040;  // 15 warps x 32 threads x 6 groups x 8 elements
-constexpr int kBulkStages = 4;
+constexpr int kBulkMaxStages = 5;             // 5 x 45 KB + the pointer cache fit for R <= 112
+constexpr size_t kMaxDynamicSmem = 231424;    // opt-in shared memory per CTA on sm_103 (232448) less 1 KB
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // bound of every device-side wait
 
 // All-gather placement kernel geometry.
@@ -91,8 +92,10 @@ int record_cuda_error(cudaError_t e);
 cudaError_t launch_reduce_scatter(const RsSeg* segs, int nsegs, int64_t nchunks,
                                   const uint16_t* const* grads, float* const* shards, int R, int P,
                                   int allow_vec, int ctas, cudaStream_t stream);
-// Bulk-copy variant: dynamic shared memory per CTA (stages + the current piece's R pointers).
-size_t bulk_smem_bytes(int R);
+// Bulk-copy variant: dynamic shared memory per CTA (stages + the current piece's R pointers), and
+// the number of stages used for R ranks.
+size_t bulk_smem_bytes(int R, int stages);
+int bulk_stages(int R);
 cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, int nsegs, int64_t nchunks, const uint16_t* const* grads,
                                        float* const* shards, int R, int P, int allow_vec, int ctas, int* status,
                                        uint64_t timeout_ns, int inject, cudaStream_t stream);
