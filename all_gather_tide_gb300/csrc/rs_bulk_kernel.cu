@@ -17,9 +17,10 @@
 //
 // One CTA = 1 producer warp (lane 0 issues the copies) + kBulkConsumerWarps consumer warps; one
 // CTA per SM.  Per stage the producer waits on the stage's `empty` mbarrier, announces the byte
-// count on its `full` mbarrier and issues one cp.async.bulk; consumers wait on `full`, add their
-// slice of the row with mixed-precision adds (add.rn.f32.bf16: the bf16 operand widened exactly,
-// the fp32 sum rounded to nearest even; one instruction per element), and release the stage.  Elements a bulk copy cannot carry (a piece whose
+// count on its `full` mbarrier and issues one cp.async.bulk; consumers wait on `full`, copy their
+// slice of the row into registers, release the stage, and then add the slice with mixed-precision
+// adds (add.rn.f32.bf16: the bf16 operand widened exactly, the fp32 sum rounded to nearest even; one
+// instruction per element).  Elements a bulk copy cannot carry (a piece whose
 // offsets are not 16-byte compatible, the < 8-element tail of the valid rows) are read with plain
 // loads, and padding is stored as zeros, exactly as in the register-path kernel: the results are
 // the same bits.
@@ -96,26 +97,32 @@ __device__ __forceinline__ void add_pair(float& acc0, float& acc1, uint32_t w) {
         : "r"(w));
 }
 
-// Adds (First: widens) this thread's groups of one rank row held in shared memory.
-template <bool First, int Groups, int Consumers>
-__device__ __forceinline__ void accumulate_row(float (&acc)[Groups][8], const uint4* row, int ctid, bool whole,
-                                               int64_t nbulk) {
+// Copies this thread's 8-element groups of one rank row from shared memory into registers (zeros for
+// groups past the copied elements, whose sums are never stored).
+template <int Groups, int Consumers>
+__device__ __forceinline__ void load_row(uint4 (&w)[Groups], const uint4* row, int ctid, bool whole, int64_t nbulk) {
 #pragma unroll
     for (int j = 0; j < Groups; ++j) {
         const int g = j * Consumers + ctid;  // 8-element group index in the chunk
-        if (whole || int64_t(g) * 8 + 8 <= nbulk) {
-            const uint4 w = row[g];
-            if (First) {
-                first_pair(acc[j][0], acc[j][1], w.x);
-                first_pair(acc[j][2], acc[j][3], w.y);
-                first_pair(acc[j][4], acc[j][5], w.z);
-                first_pair(acc[j][6], acc[j][7], w.w);
-            } else {
-                add_pair(acc[j][0], acc[j][1], w.x);
-                add_pair(acc[j][2], acc[j][3], w.y);
-                add_pair(acc[j][4], acc[j][5], w.z);
-                add_pair(acc[j][6], acc[j][7], w.w);
-            }
+        w[j] = (whole || int64_t(g) * 8 + 8 <= nbulk) ? row[g] : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Adds (First: widens) one rank row's groups held in registers.
+template <bool First, int Groups>
+__device__ __forceinline__ void add_row(float (&acc)[Groups][8], const uint4 (&w)[Groups]) {
+#pragma unroll
+    for (int j = 0; j < Groups; ++j) {
+        if (First) {
+            first_pair(acc[j][0], acc[j][1], w[j].x);
+            first_pair(acc[j][2], acc[j][3], w[j].y);
+            first_pair(acc[j][4], acc[j][5], w[j].z);
+            first_pair(acc[j][6], acc[j][7], w[j].w);
+        } else {
+            add_pair(acc[j][0], acc[j][1], w[j].x);
+            add_pair(acc[j][2], acc[j][3], w[j].y);
+            add_pair(acc[j][4], acc[j][5], w[j].z);
+            add_pair(acc[j][6], acc[j][7], w[j].w);
         }
     }
 }
@@ -329,10 +336,14 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nc
             for (int r = 0; r < R; ++r) {
                 if (!wait_bounded(&full[s], phase, timeout_ns, abort, status, 1)) return;
                 const uint4* row = reinterpret_cast<const uint4*>(data + int64_t(s) * kBulkChunk * 2);
-                if (r == 0) accumulate_row<true, kGroups, kConsumers>(acc, row, ctid, whole, v.nbulk);
-                else accumulate_row<false, kGroups, kConsumers>(acc, row, ctid, whole, v.nbulk);
+                // release the stage as soon as the warp's slice is in registers, before the adds, so
+                // the producer can refill it while the adds run
+                uint4 w[kGroups];
+                load_row<kGroups, kConsumers>(w, row, ctid, whole, v.nbulk);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
+                if (r == 0) add_row<true, kGroups>(acc, w);
+                else add_row<false, kGroups>(acc, w);
                 if (++s == stages) {
                     s = 0;
                     phase ^= 1u;
