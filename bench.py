@@ -21,6 +21,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -357,6 +358,8 @@ def run_tide(args, rank, world, local_rank):
         out["e2e"]["host_affinity"] = numa
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(g, dev, reps=args.cpu_reps)
+        out["cpu_baseline"]["cpu_model"] = cpu_model()
+        out["cpu_baseline_all_cores"] = cpu_baseline_all_cores(g, dev)
     G.close()
     return out
 
@@ -856,8 +859,8 @@ def end_to_end(G, g, buf, S, U, dev, args, world):
 # ---- the host oracle ---------------------------------------------------------------------------
 
 
-def cpu_sample(g: Group):
-    params = tuple(p for p in g.params if p[0] in CPU_SAMPLE_PARAMS) or g.params[:1]
+def cpu_sample(g: Group, names=CPU_SAMPLE_PARAMS):
+    params = tuple(p for p in g.params if p[0] in names) or g.params[:1]
     return Group(g.name + "-sample", g.R, params, g.grad_kind, g.grad_sigma, g.shard_sigma, g.grad_seed,
                  g.grad_seed_per_rank, g.shard_seed_base)
 
@@ -894,6 +897,69 @@ def cpu_baseline(g: Group, dev, reps: int = 4):
                       f"({lay.U} of the group's elements per rank-set; reduce-scatter + all-gather, "
                       f"{reps} passes), single-threaded C oracle",
             "host_cpus": os.cpu_count()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the baseline's record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=30).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.processor() or platform.machine()
+
+
+def _oracle_replica(sub: Group, grads, shards, reps: int, barrier, results) -> None:
+    """One host process of the all-cores baseline: the unchanged single-threaded oracle on its own
+    copy of the sample's inputs, started with the others through a barrier."""
+    import oracle
+
+    lay = oracle.plan(sub.R, sub.rows, sub.row_len)
+    params = [np.empty(sub.numel(p), np.uint16) for p in range(sub.P)]
+    oracle_step(oracle, lay, grads, shards, params)  # warm
+    barrier.wait(timeout=600)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(oracle, lay, grads, shards, params)
+    results.put(time.perf_counter() - t0)
+
+
+def cpu_baseline_all_cores(g: Group, dev=None, reps: int = 8) -> dict:
+    """The oracle on every host core this process may use: one replica process per core (spawned,
+    never forked from a CUDA process), each running the single-threaded oracle over the k and v
+    matrices of the layer on its own copy of the inputs (drawn once here and sent to each replica);
+    value = the bytes all replicas moved / the slowest replica's time."""
+    import multiprocessing as mp
+
+    import oracle
+
+    oracle.build()
+    n = len(os.sched_getaffinity(0))
+    sub = cpu_sample(g, ("k", "v"))
+    lay = oracle.plan(sub.R, sub.rows, sub.row_len)
+    grads, shards = cpu_inputs(sub, lay.S, dev)
+    nbytes = rs_bytes(sub, lay.S, lay.U) + ag_bytes(lay.U)
+    ctx = mp.get_context("spawn")
+    barrier, results = ctx.Barrier(n), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_replica, args=(sub, grads, shards, reps, barrier, results), daemon=True)
+             for _ in range(n)]
+    for p in procs:
+        p.start()
+    try:
+        times = [results.get(timeout=900) for _ in range(n)]
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+            if p.is_alive():
+                p.kill()
+    return {"value": n * nbytes * reps / max(times) / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+            "seconds": max(times),
+            "sample": f"{n} processes, each the single-threaded C oracle on its own copy of {g.name} restricted "
+                      f"to {', '.join(p[0] for p in sub.params)} ({lay.U} elements per rank-set; reduce-scatter "
+                      f"+ all-gather, {reps} passes)",
+            "cpu_model": cpu_model()}
 
 
 def run_reference(args):

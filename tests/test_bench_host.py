@@ -67,3 +67,11 @@ def test_reference_arm_json_contract():
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_all_cores_baseline_runs_one_replica_per_core():
+    g = group("llama8b").scaled(8)
+    res = bench.cpu_baseline_all_cores(g, None, reps=2)
+    assert res["kind"] == "oracle" and res["unit"] == "GB/s" and res["value"] > 0
+    assert res["cores"] == len(os.sched_getaffinity(0))
+    assert "k, v" in res["sample"] and res["cpu_model"]
