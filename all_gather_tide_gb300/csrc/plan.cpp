@@ -77,10 +77,13 @@ void make_work_lists(Plan* pl) {
 
     // The same pieces cut into the bulk-copy kernel's larger chunks.
     pl->rs_bulk.clear();
+    pl->rs_bulk_piece.clear();
     chunks = 0;
     for (RsSeg sg : pl->rs) {
         sg.chunk_begin = chunks;
-        chunks += (sg.total + kBulkChunk - 1) / kBulkChunk;
+        const int64_t n = (sg.total + kBulkChunk - 1) / kBulkChunk;
+        chunks += n;
+        pl->rs_bulk_piece.insert(pl->rs_bulk_piece.end(), size_t(n), int32_t(pl->rs_bulk.size()));
         pl->rs_bulk.push_back(sg);
     }
     pl->rs_bulk_chunks = chunks;

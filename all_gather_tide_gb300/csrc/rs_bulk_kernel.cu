@@ -142,26 +142,6 @@ __device__ __forceinline__ float sum_scalar(const uint16_t* const* __restrict__ 
     return acc;
 }
 
-__device__ __forceinline__ int find_piece(const RsSeg* __restrict__ segs, int nsegs, int cur, int64_t c) {
-    if (cur + 1 >= nsegs || segs[cur + 1].chunk_begin > c) return cur;
-    int lo = cur + 1, hi = nsegs, step = 1;
-    for (;;) {
-        const int nxt = lo + step;
-        if (nxt >= nsegs) break;
-        if (segs[nxt].chunk_begin > c) {
-            hi = nxt;
-            break;
-        }
-        lo = nxt;
-        step <<= 1;
-    }
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (segs[mid].chunk_begin <= c) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
 // Chunk geometry shared by producer and consumers.
 struct ChunkView {
     int64_t n;       // elements in the chunk
@@ -195,18 +175,21 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uin
     return true;
 }
 
-// The piece holding the current chunk, cached across the chunks of one piece (chunks only move
-// forward), so a chunk normally costs no table load at all.
+// The piece holding the current chunk, cached across the chunks of one piece: while the chunk stays
+// inside the cached piece the cursor costs nothing; when it leaves, one load from the planner's
+// chunk -> piece table finds the new piece (the CTAs' chunks are a grid stride apart, so with many
+// small pieces a search of the piece list would cost a chain of dependent loads per chunk).
 struct PieceCursor {
     int cur = -1;
-    int64_t next_begin = 0;  // first chunk of the next piece
+    int64_t next_begin = 0;  // first chunk after the cached piece
     int64_t dst_off = 0, src_off = 0, valid = 0, total = 0, chunk_begin = 0;
     int d = 0, p = 0, vec = 0;
 
-    // Moves to the piece holding chunk c; true when it changed.
-    __device__ __forceinline__ bool seek(const RsSeg* __restrict__ segs, int nsegs, int64_t c) {
+    // Moves to the piece holding chunk c (chunks only move forward); true when it changed.
+    __device__ __forceinline__ bool seek(const RsSeg* __restrict__ segs, const int32_t* __restrict__ chunk_piece,
+                                         int64_t c) {
         if (cur >= 0 && c < next_begin) return false;
-        cur = find_piece(segs, nsegs, cur < 0 ? 0 : cur, c);
+        cur = __ldg(&chunk_piece[c]);
         const RsSeg* q = segs + cur;
         dst_off = __ldg(&q->dst_off);
         src_off = __ldg(&q->src_off);
@@ -216,7 +199,7 @@ struct PieceCursor {
         d = __ldg(&q->d);
         p = __ldg(&q->p);
         vec = __ldg(&q->vec);
-        next_begin = cur + 1 < nsegs ? __ldg(&segs[cur + 1].chunk_begin) : INT64_MAX;
+        next_begin = chunk_begin + (total + kBulkChunk - 1) / kBulkChunk;
         return true;
     }
 
@@ -241,7 +224,7 @@ __device__ __forceinline__ void st_cs_v8(float* p, const float (&a)[8]) {
 }
 
 __global__ void __launch_bounds__(kBulkThreads, 1)
-reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nchunks,
+reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, const int32_t* __restrict__ chunk_piece, int64_t nchunks,
                            const uint16_t* const* __restrict__ grads, float* const* __restrict__ shards, int R,
                            int P, int allow_vec, int stages, int* status, uint64_t timeout_ns, int inject) {
     constexpr int kConsumers = kBulkConsumerWarps * 32;
@@ -274,7 +257,7 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nc
         int s = 0;            // stage of use `it`
         uint32_t phase = 0;   // its phase parity
         for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-            if (pc.seek(segs, nsegs, c)) {
+            if (pc.seek(segs, chunk_piece, c)) {
                 for (int r = lane; r < R; r += 32) gptr[r] = grads[int64_t(r) * P + pc.p];
                 __syncwarp();
             }
@@ -327,7 +310,7 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nc
     int s = 0;
     uint32_t phase = 0;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        if (pc.seek(segs, nsegs, c)) shard = shards[pc.d];
+        if (pc.seek(segs, chunk_piece, c)) shard = shards[pc.d];
         const ChunkView v = pc.view(c, kBulkChunk, allow_vec);
         float* __restrict__ dst = shard + v.dst;
         if (v.nbulk > 0) {
@@ -382,7 +365,8 @@ int bulk_stages(int R) {
     return 0;
 }
 
-cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, int nsegs, int64_t nchunks, const uint16_t* const* grads,
+cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, const int32_t* chunk_piece, int64_t nchunks,
+                                       const uint16_t* const* grads,
                                        float* const* shards, int R, int P, int allow_vec, int ctas, int* status,
                                        uint64_t timeout_ns, int inject, cudaStream_t stream) {
     if (nchunks <= 0) return cudaSuccess;
@@ -393,7 +377,7 @@ cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, int nsegs, int64_t nch
                                          int(smem));
     if (e != cudaSuccess) return e;
     const int grid = int(std::min<int64_t>(ctas, nchunks));
-    reduce_scatter_bulk_kernel<<<grid, kBulkThreads, smem, stream>>>(segs, nsegs, nchunks, grads, shards, R, P,
+    reduce_scatter_bulk_kernel<<<grid, kBulkThreads, smem, stream>>>(segs, chunk_piece, nchunks, grads, shards, R, P,
                                                                      allow_vec, stages, status, timeout_ns, inject);
     return cudaGetLastError();
 }

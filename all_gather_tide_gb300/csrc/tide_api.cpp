@@ -58,6 +58,7 @@ struct tide_group {
     int* d_status = nullptr;  // device status word written by bounded waits that expire
     tide::RsSeg* d_rs = nullptr;
     tide::RsSeg* d_rs_bulk = nullptr;
+    int32_t* d_rs_bulk_piece = nullptr;  // piece index of every bulk chunk
     tide::AgSeg* d_ag_bulk = nullptr;
     tide::AgSeg* d_ag = nullptr;
     size_t slot_cap = 0;
@@ -96,6 +97,7 @@ void release(tide_group* g) {
     if (g->fork) cudaEventDestroy(g->fork);
     if (g->d_rs) cudaFree(g->d_rs);
     if (g->d_rs_bulk) cudaFree(g->d_rs_bulk);
+    if (g->d_rs_bulk_piece) cudaFree(g->d_rs_bulk_piece);
     if (g->d_ag_bulk) cudaFree(g->d_ag_bulk);
     if (g->d_status) cudaFree(g->d_status);
     if (g->d_ag) cudaFree(g->d_ag);
@@ -198,7 +200,7 @@ int default_ctas(const tide_group* g, int per_sm) { return std::max(1, g->sm_cou
 // register path's element-wise fallback covers the rest).  Measured on GB300 it is the faster of
 // the two at every CTA count, most of all when the count is capped below the SM count.
 bool use_bulk(const tide_group* g, bool aligned) {
-    if (!aligned || g->plan.rs_bulk.empty() || !g->d_rs_bulk) return false;
+    if (!aligned || g->plan.rs_bulk.empty() || !g->d_rs_bulk || !g->d_rs_bulk_piece) return false;
     return g->rs_variant != TIDE_RS_REGISTER;
 }
 
@@ -245,7 +247,11 @@ int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* ro
     int rc = tide::make_layout(R, P, rows, row_len, &pl);
     if (rc != TIDE_OK) return rc;
     if (int64_t(R) * P > TIDE_MAX_TABLE) return TIDE_ERANGE;
-    tide::make_work_lists(&pl);
+    try {
+        tide::make_work_lists(&pl);
+    } catch (const std::bad_alloc&) {
+        return TIDE_ENOMEM;
+    }
 
     tide_group* g = new (std::nothrow) tide_group();
     if (!g) return TIDE_ENOMEM;
@@ -270,6 +276,10 @@ int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* ro
         e = cudaMalloc(&g->d_rs_bulk, rb.size() * sizeof(tide::RsSeg));
         if (e == cudaSuccess)
             e = cudaMemcpy(g->d_rs_bulk, rb.data(), rb.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
+        const auto& rp = g->plan.rs_bulk_piece;
+        if (e == cudaSuccess) e = cudaMalloc(&g->d_rs_bulk_piece, rp.size() * sizeof(int32_t));
+        if (e == cudaSuccess)
+            e = cudaMemcpy(g->d_rs_bulk_piece, rp.data(), rp.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
     }
     const auto& ab = g->plan.ag_bulk;
     if (e == cudaSuccess && !ab.empty()) {
@@ -373,7 +383,7 @@ int tide_reduce_scatter(tide_group_t g, const void* const* grads, void* const* s
     cudaError_t e;
     if (use_bulk(g, aligned)) {
         const int ctas = g->rs_ctas ? g->rs_ctas : g->sm_count;
-        e = tide::launch_reduce_scatter_bulk(g->d_rs_bulk, int(g->plan.rs_bulk.size()), g->plan.rs_bulk_chunks, gp, sp,
+        e = tide::launch_reduce_scatter_bulk(g->d_rs_bulk, g->d_rs_bulk_piece, g->plan.rs_bulk_chunks, gp, sp,
                                              R, P, 1, ctas, g->d_status, g->timeout_ns,
                                              (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
     } else {

@@ -74,6 +74,7 @@ struct Plan {
     int64_t rs_chunks = 0;
     std::vector<RsSeg> rs_bulk;  // same pieces, chunked for the bulk-copy kernel
     int64_t rs_bulk_chunks = 0;
+    std::vector<int32_t> rs_bulk_piece;  // index in rs_bulk of every bulk chunk's piece
     std::vector<AgSeg> ag;
     int64_t ag_chunks = 0;
     std::vector<AgSeg> ag_bulk;  // same runs, chunked for the bulk-copy placement kernel
@@ -96,7 +97,8 @@ cudaError_t launch_reduce_scatter(const RsSeg* segs, int nsegs, int64_t nchunks,
 // the number of stages used for R ranks.
 size_t bulk_smem_bytes(int R, int stages);
 int bulk_stages(int R);
-cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, int nsegs, int64_t nchunks, const uint16_t* const* grads,
+cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, const int32_t* chunk_piece, int64_t nchunks,
+                                       const uint16_t* const* grads,
                                        float* const* shards, int R, int P, int allow_vec, int ctas, int* status,
                                        uint64_t timeout_ns, int inject, cudaStream_t stream);
 size_t ag_bulk_smem_bytes();
