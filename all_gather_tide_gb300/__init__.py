@@ -112,6 +112,16 @@ def _ptr(x) -> int:
 
 
 def _ptr_array(xs: Sequence) -> ctypes.Array:
+    if isinstance(xs, ctypes.Array):  # already marshalled (see pointer_table)
+        return xs
+    return (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+
+
+def pointer_table(xs: Sequence) -> ctypes.Array:
+    """Marshals tensors (or raw addresses) once into the pointer array the C calls take, for callers
+    that pass the same buffers every step: a group with hundreds of parameters otherwise pays about
+    a millisecond of Python per call to read R*P data pointers.  The tensors must stay alive and
+    unmoved while the table is in use."""
     return (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
 
 
@@ -199,7 +209,9 @@ def tide_group_get_ctas(g: int) -> Tuple[int, int]:
     return a.value, b.value
 
 
-def _flat_grads(grads) -> List:
+def _flat_grads(grads):
+    if isinstance(grads, ctypes.Array):
+        return grads
     if len(grads) and isinstance(grads[0], (list, tuple)):
         return [x for row in grads for x in row]
     return list(grads)

@@ -432,10 +432,23 @@ def stock_comparator(G, g, buf, S, U, stream, legs):
 
     rs_ms, ag_ms = timed(rs), timed(ag)
     b_rs, b_ag = rs_bytes(g, S, U), ag_bytes(U)
+    # SM time (SMs held x duration), the pages' measure of what a collective takes from compute:
+    # the stock ops each fill the GPU; the direct path holds its CTA count (one CTA per SM)
+    sms = torch.cuda.get_device_properties(buf.shards.device).multi_processor_count
+    rs_ctas0, ag_ctas0 = G.get_ctas()
+    G.set_ctas(16, ag_ctas0)
+    ms16 = timed(lambda: G.reduce_scatter(buf.grads, buf.shard_list))
+    G.set_ctas(rs_ctas0, ag_ctas0)
+    direct_ms, direct_ctas = legs["reduce_scatter"]["ms"], legs["reduce_scatter"]["ctas"]
+    sm_time = {"stock_sm_ms": rs_ms * sms, "direct_sm_ms": direct_ms * min(direct_ctas, sms),
+               "direct_16ctas_ms": ms16, "direct_16ctas_sm_ms": ms16 * 16,
+               "ratio_full_width": rs_ms * sms / (direct_ms * min(direct_ctas, sms)),
+               "ratio_16ctas": rs_ms * sms / (ms16 * 16)}
     res = {
         "reduce_scatter": {"ms": rs_ms, "gbs_of_direct_bytes": b_rs / (rs_ms * 1e-3) / 1e9,
                            "direct_ms": legs["reduce_scatter"]["ms"], "speedup_direct": rs_ms / legs["reduce_scatter"]["ms"],
-                           "extra_buffer_bytes": packed.numel() * 4, "pack": "torch._chunk_cat" if have_chunk_cat else "chunk+copy"},
+                           "extra_buffer_bytes": packed.numel() * 4, "pack": "torch._chunk_cat" if have_chunk_cat else "chunk+copy",
+                           "sm_time": sm_time},
         "all_gather_copy_out": {"ms": ag_ms, "gbs_of_direct_bytes": b_ag / (ag_ms * 1e-3) / 1e9,
                                 "direct_ms": legs["all_gather_sm"]["ms"], "speedup_direct": ag_ms / legs["all_gather_sm"]["ms"],
                                 "op": "torch.split_with_sizes_copy into padded [R, m_p*L_p] storage"},

@@ -108,3 +108,14 @@ def test_probe_argument_checks_before_cuda(tide):
     assert L.tide_probe_bulk_read(None, 1024, 1, 4096, 4, None, None) == tide.TIDE_EINVAL
     assert L.tide_probe_bulk_read(16, 1024, 1, 4095, 4, 16, None) == tide.TIDE_EINVAL
     assert L.tide_probe_bulk_read(16, 1024, 1, 65536, 4, 16, None) == tide.TIDE_EINVAL  # > 200 KB staged
+
+
+def test_pointer_table_marshalling(tide):
+    import torch
+
+    xs = [torch.empty(3, dtype=torch.int16) for _ in range(5)] + [12345]
+    t = tide.pointer_table(xs)
+    assert [v for v in t] == [x.data_ptr() for x in xs[:5]] + [12345]
+    assert tide._ptr_array(t) is t and tide._flat_grads(t) is t
+    L = tide.lib()
+    assert L.tide_reduce_scatter(None, t, t, None) == tide.TIDE_EINVAL

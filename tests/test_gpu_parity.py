@@ -374,6 +374,34 @@ def test_pointer_table_ring_and_streams(tide):
     G.close()
 
 
+def test_premarshalled_pointer_tables(tide):
+    """Pointer tables marshalled once with pointer_table give the same bits as tensor lists, for
+    the reduce-scatter and both placements, on a many-parameter group."""
+    g = group("qwen3moe").scaled(16)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    host = rng.group_grads(g)
+    want = oracle.reduce_scatter(lay, [[t.numpy().view(np.uint16) for t in row] for row in host])
+    dev = [[t.cuda() for t in row] for row in host]
+    out = [torch.full((lay.S,), float("nan"), device="cuda") for _ in range(g.R)]
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+    gt = tide.pointer_table([t for row in dev for t in row])
+    st = tide.pointer_table(out)
+    for _ in range(2):
+        G.reduce_scatter(gt, st)
+    torch.cuda.synchronize()
+    for d in range(g.R):
+        assert np.array_equal(f32_bits(out[d]), want[d].view(np.uint32)), d
+    shards = [rng.shard_bits(g, r, lay.S).cuda() for r in range(g.R)]
+    ref = [torch.empty(g.numel(p), dtype=torch.int16, device="cuda") for p in range(g.P)]
+    G.all_gather(shards, ref)
+    for ce in (False, True):
+        got = [torch.zeros(g.numel(p), dtype=torch.int16, device="cuda") for p in range(g.P)]
+        (G.all_gather_ce if ce else G.all_gather)(tide.pointer_table(shards), tide.pointer_table(got))
+        torch.cuda.synchronize()
+        assert all(torch.equal(a, b) for a, b in zip(got, ref)), ce
+    G.close()
+
+
 # ---- full sizes, launch configuration of the benchmark ---------------------------------------
 
 FULL = ["llama8b", "qwen3moe", "llama70b", "wan_r8", "wan_r16", "wan_r32", "wan_r64"]
