@@ -143,7 +143,10 @@ int tide_all_gather(tide_group_t g, const void *const *shards, void *const *para
  * tide_all_gather_ce — the same placement with copy engines and no SM kernel (Table 1 "AG SM
  * budget 0"; Fig. 5b).  By default one cudaMemcpyAsync per (rank, parameter) run of valid rows,
  * spread over the group's copy-engine lanes (tide_group_set_ce_lanes; default 8): measured on
- * GB300 this is the fast form.  With TIDE_FLAG_CE_2D, and when shards[r] = shards[0] + r*pitch for
+ * GB300 this is the fast form for runs of several MB (Llama-3.1-70B layer: 6.4 TB/s), but the host
+ * spends ~2 us submitting each copy, so groups of hundreds of short runs (Qwen3 MoE layer: 3,144
+ * copies, 0.37 TB/s) do better with the 2-D form (2.6 TB/s there, ~3.5 TB/s on the other groups).
+ * With TIDE_FLAG_CE_2D, and when shards[r] = shards[0] + r*pitch for
  * one pitch >= S*2 bytes, each parameter instead takes the paper's one strided copy: one
  * cudaMemcpy2DAsync over its full ranks (height f_p = floor(rows_p/m_p), width s_p*2 bytes) plus at
  * most one cudaMemcpyAsync for the rank holding its last partial piece; without a uniform pitch it
