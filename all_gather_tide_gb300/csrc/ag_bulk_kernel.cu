@@ -1,8 +1,8 @@
 // All-gather placement with bulk asynchronous copies (sm_103a).
 //
-// Paper: "The Endgame of FSDP Communication" (arXiv 2610.38228).  TIDE-AG lands shards directly in
-// parameter storage with copy engines and no SM work (abstract; Table 1 "AG SM budget 0"; Fig. 5b one
-// strided copy per parameter).  This kernel is the closest SM-side form: one thread per CTA drives
+// Paper: "The Endgame of FSDP Communication" (arXiv 2610.38228).  the paper's all-gather puts shards
+// into the parameters' storage with copy engines and no SM work (abstract; Table 1, no SM for the
+// all-gather; Fig. 5b, a single strided copy for each parameter).  This kernel is the closest SM-side form: one thread per CTA drives
 // the SM's bulk-copy engine, moving each run of valid elements shard_r[o_p ..) -> param_p[r*s_p ..)
 // through shared memory (cp.async.bulk global -> shared, then cp.async.bulk shared -> global), so a
 // CTA spends almost no issue slots and few CTAs still move a lot of data.

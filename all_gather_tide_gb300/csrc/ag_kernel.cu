@@ -2,7 +2,7 @@
 //
 // Paper: "The Endgame of FSDP Communication" (arXiv 2610.38228).  The abstract's TIDE-AG lands
 // gathered shards directly in per-parameter storage instead of copying a flat rank-major buffer
-// out afterwards (Table 7 "+ Copy-out"); Fig. 5b does it with one strided copy per parameter.
+// out afterwards (Table 7, the copy-out column); Fig. 5b does it with a single strided copy for each parameter.
 // This kernel is the SM form of that placement: for every (source rank r, parameter p) the
 // planner emits the run of valid elements, shard_r[o_p, o_p + v(r,p)*L_p) -> param_p[r*s_p, ...),
 // cut into chunks of kAgChunk elements; CTAs walk the chunk list with a grid stride.  Each

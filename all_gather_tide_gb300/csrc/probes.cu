@@ -2,8 +2,8 @@
 //
 // Paper: "The Endgame of FSDP Communication" (arXiv 2610.38228).  Fig. 4 measures how a GEMM slows
 // as spin kernels keep a growing number of CTAs resident; Table 5 (and Fig. 3) use an SM-id probe:
-// CTAs shaped like the GEMM's clusters, each filling an SM, record their SM id and entry and exit
-// times, so CTAs displaced past the first wave, and the SMs a collective keeps, can be counted.
+// CTAs shaped like the GEMM's clusters, each occupying a whole SM, write down the SM number and
+// the arrival and departure times, so CTAs displaced past the first wave, and the SMs a collective keeps, can be counted.
 // A third probe measures how fast one SM's bulk-copy engine reads as a function of the copy size,
 // the fact the bulk-copy reduce-scatter is built around.
 //

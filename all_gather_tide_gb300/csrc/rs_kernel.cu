@@ -1,8 +1,8 @@
 // Layout-aware mixed-precision reduce-scatter kernel (sm_103a).
 //
-// Paper: "The Endgame of FSDP Communication" (arXiv 2610.38228).  The abstract's TIDE-RS reads
-// per-parameter bf16 gradients in place (Table 1 "In-Place Read", no full-group pack) and
-// reduces them into fp32 shards; Fig. 2b step 5 forms the fp32 sums with a bounded number of
+// Paper: "The Endgame of FSDP Communication" (arXiv 2610.38228).  The paper's reduce-scatter
+// takes each parameter's bf16 gradient where it lies (Table 1, the in-place read row: no
+// full-group pack) and sums into fp32 shards (abstract); Fig. 2b step 5 forms the fp32 sums with a bounded number of
 // short-lived CTAs.  On one GPU every contributor rank is a buffer in local HBM, so the sum CTAs
 // read the R gradients directly, and the landing step is folded into the same pass: each fp32
 // result is stored once, at its final address in the destination shard (Fig. 1).

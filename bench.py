@@ -9,8 +9,8 @@ and larger than L2 (17.1 GB of reduce-scatter traffic per step), so no L2 flush 
 Printed (rank 0, one JSON line): the effective HBM GB/s of the step (algorithmic bytes / time),
 per-leg GB/s and fraction of the measured HBM peak (reduce-scatter, SM placement, copy-engine
 placement), the roofline of the dominant kernel (reduce-scatter), the end-to-end figure through
-the C ABI with host buffers, the slowdown of a concurrent single-wave cuBLAS bf16 GEMM
-(4096 x 4096 x 8192) on another stream, SM clocks sampled during the timed region, and the CPU
+the C ABI with host buffers, how much a single-wave cuBLAS bf16 GEMM (4096 x 4096 x 8192)
+running beside the collective on another stream slows down, SM clocks sampled during the timed region, and the CPU
 oracle timed on the host on a bounded sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tide|reference] [--workload NAME]
@@ -385,8 +385,8 @@ def time_ce(G, buf, stream, b_ag, iters):
 
 
 def stock_comparator(G, g, buf, S, U, stream, legs):
-    """The layout-converting path the paper compares against (Table 1 "Full-group pack", Table 7
-    "+ Copy-out", Table 8 "FSDP2 columns include _chunk_cat"), emulated on one GPU with plain
+    """The layout-converting path the paper compares against (Table 1's full-group pack, Table 7's
+    copy-out column, Table 8, whose FSDP2 numbers count the _chunk_cat pack), emulated on one GPU with plain
     PyTorch ops: every contributor packs its per-parameter bf16 gradients into a full-group fp32
     buffer ([R, S] per contributor, zero padding; torch._chunk_cat as FSDP2 does), the packed
     buffers are summed per destination (the reduce-scatter), and the all-gather output, a flat
@@ -464,8 +464,8 @@ def stock_comparator(G, g, buf, S, U, stream, legs):
 
 
 def slot_reuse(G, g, buf, S, U, stream):
-    """Slot-Reuse on one GPU: every rank's gradients are copied (copy engines) into a vacated
-    all-gather slot of R*S bf16 elements, after which the gradient tensors could be released; the
+    """Slot-Reuse on one GPU: every rank's gradients are copied (copy engines) into an
+    all-gather slot no longer in use of R*S bf16 elements, after which the gradient tensors could be released; the
     reduce-scatter then reads the slots.  Reports the staging time, the reduce-scatter from the
     slots, and the gradient bytes that become free once staging is enqueued."""
     slots = torch.empty(g.R, g.R * S, dtype=torch.bfloat16, device=buf.shards.device)

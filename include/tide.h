@@ -111,9 +111,9 @@ int tide_group_get_ctas(tide_group_t g, int32_t *rs_ctas, int32_t *ag_ctas);
 
 /* ---- collectives ------------------------------------------------------------------------- */
 /*
- * tide_reduce_scatter — layout-aware mixed-precision reduce-scatter (abstract: TIDE-RS consumes
- * per-parameter bf16 gradients directly and reduces them into fp32 shards; Table 1 "In-Place
- * Read"; Fig. 2b step 5).  For every destination rank d and parameter p:
+ * tide_reduce_scatter — layout-aware mixed-precision reduce-scatter (abstract: the reduce-scatter
+ * takes each parameter's bf16 gradient tensor as it is and sums into fp32 shards; Table 1, the
+ * in-place read row; Fig. 2b step 5).  For every destination rank d and parameter p:
  *     shard_d[o_p + i] = g_0[i'] + g_1[i'] + ... + g_{R-1}[i'],  i' = d*s_p + i,  i < v(d,p)*L_p
  *     shard_d[o_p + i] = +0.0f                                   v(d,p)*L_p <= i < s_p
  * where g_r is rank r's bf16 gradient of p, widened exactly to fp32 and added in ascending
@@ -129,8 +129,8 @@ int tide_reduce_scatter(tide_group_t g, const void *const *grads, void *const *s
                         void *stream);
 
 /*
- * tide_all_gather — all-gather placement, SM kernel (abstract: TIDE-AG delivers shards
- * directly to parameter storage; Fig. 1; Fig. 5b).  For every rank r and parameter p:
+ * tide_all_gather — all-gather placement, SM kernel (abstract: the all-gather lands each shard
+ * in the parameters' own storage, with no copy-out; Fig. 1; Fig. 5b).  For every rank r and parameter p:
  *     param_p[r*s_p + i] = shard_r[o_p + i]      for i < v(r,p)*L_p
  * Padding elements of the shards are never read; nothing outside the params is written.
  *   shards: host array of R device pointers, entry r = rank r's packed bf16 shard (S elements).
@@ -140,8 +140,8 @@ int tide_all_gather(tide_group_t g, const void *const *shards, void *const *para
                     void *stream);
 
 /*
- * tide_all_gather_ce — the same placement with copy engines and no SM kernel (Table 1 "AG SM
- * budget 0"; Fig. 5b).  By default one cudaMemcpyAsync per (rank, parameter) run of valid rows,
+ * tide_all_gather_ce — the same placement with copy engines and no SM kernel (Table 1: the
+ * all-gather takes no SM; Fig. 5b).  By default one cudaMemcpyAsync per (rank, parameter) run of valid rows,
  * spread over the group's copy-engine lanes (tide_group_set_ce_lanes; default 8): measured on
  * GB300 this is the fast form for runs of several MB (Llama-3.1-70B layer: 6.4 TB/s), but the host
  * spends ~2 us submitting each copy, so groups of hundreds of short runs (Qwen3 MoE layer: 3,144
@@ -194,8 +194,8 @@ int tide_group_device_status(tide_group_t g, int32_t *status);
 int tide_group_set_debug(tide_group_t g, uint32_t flags);
 
 /*
- * tide_stage_into_slots — Slot-Reuse staging (abstract: "Slot-Reuse optionally stages gradients
- * in vacated all-gather slots"; Fig. 7: the gradients are copied into a vacated all-gather slot and
+ * tide_stage_into_slots — Slot-Reuse staging (abstract: an optional mode that parks the gradients
+ * in all-gather slots that are no longer in use; Fig. 7: the gradients are copied into a vacated slot and
  * the slot's reuse is gated on read completion).  For every rank r it copies the P gradients of
  * grads[r*P + p] with copy engines (one cudaMemcpyAsync each, stream-ordered) into slots[r], packed
  * in parameter order without padding (parameter p at element rows_0*L_0 + ... + rows_{p-1}*L_{p-1}),
@@ -260,7 +260,7 @@ int tide_reduce_scatter_noalloc(int32_t R, int32_t P, const int64_t *rows, const
  * dynamic shared memory (so a large value keeps one CTA per SM, like a GEMM CTA), in clusters of
  * `cluster_size` (1..8), that keep their SM for `hold_ns` (<= 10 s).  Fig. 4's resident spin
  * kernels and Table 5's SM-id probe: with `records` (device, 3*ctas uint64) each CTA writes its
- * SM id, entry and exit %globaltimer values, so CTAs that could not start in the first wave are
+ * SM number and its %globaltimer values on arrival and departure, so CTAs that could not start in the first wave are
  * visible.  Asynchronous on `stream`; TIDE_EINVAL on bad sizes.
  */
 int tide_probe_hold(int32_t ctas, int32_t threads, int32_t smem_bytes, int32_t cluster_size, uint64_t hold_ns,

@@ -8,13 +8,14 @@
  *
  * "TIDE" below is the paper "The Endgame of FSDP Communication: Layout-Aware Collectives on Copy
  * Engines, RDMA, and NVSwitch" (arXiv 2610.38228).  What it fixes:
- *   - abstract: FSDP2 keeps parameters and gradients as per-parameter tensors; TIDE-RS reads the
- *     per-parameter bf16 gradients directly and reduces them into fp32 shards; TIDE-AG delivers
- *     shards directly into parameter storage.
- *   - Fig. 1: each parameter is split on dim 0 into per-rank pieces; every piece is written once,
- *     at its final address.
- *   - Table 2 (notation): padded per-rank rows and row length of parameter p, per-rank shard size
- *     and prefix offset of p, per-rank packed shard size, unsharded group size.
+ *   - abstract: FSDP2 stores each parameter and its gradient as its own tensor; the reduce-scatter
+ *     takes those bf16 tensors as they are and sums them into fp32 shards; the all-gather writes
+ *     the shards straight into the parameters' storage.
+ *   - Fig. 1: each parameter is cut on dim 0 into one piece per rank, and each piece goes to its
+ *     destination in a single write.
+ *   - Table 2 (notation): for parameter p, the rows each rank holds after padding, the length of a
+ *     row, the elements of p in one rank's shard and where they start; the size of one rank's
+ *     whole shard and of the unsharded group.
  * Readings taken where the pages are silent (the symbols of Table 2 are lost in the text):
  *   - padded rows  m_p = ceil(rows_p / R)  (FSDP2 / torch.chunk dim-0 sharding);
  *   - per-rank shard  s_p = m_p * L_p  elements, prefix offset  o_p = sum_{q<p} s_q  (tight packing,
