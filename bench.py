@@ -924,14 +924,15 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def _oracle_replica(sub: Group, grads, shards, reps: int, barrier, results) -> None:
-    """One host process of the all-cores baseline: the unchanged single-threaded oracle on its own
+def _oracle_replica(sub: Group, grads, shards, reps: int, warmup: int, barrier, results) -> None:
+    """One host process of an all-cores oracle run: the unchanged single-threaded oracle on its own
     copy of the sample's inputs, started with the others through a barrier."""
     import oracle
 
     lay = oracle.plan(sub.R, sub.rows, sub.row_len)
     params = [np.empty(sub.numel(p), np.uint16) for p in range(sub.P)]
-    oracle_step(oracle, lay, grads, shards, params)  # warm
+    for _ in range(max(1, warmup)):
+        oracle_step(oracle, lay, grads, shards, params)
     barrier.wait(timeout=600)
     t0 = time.perf_counter()
     for _ in range(reps):
@@ -939,7 +940,7 @@ def _oracle_replica(sub: Group, grads, shards, reps: int, barrier, results) -> N
     results.put(time.perf_counter() - t0)
 
 
-def cpu_baseline_all_cores(g: Group, dev=None, reps: int = 8) -> dict:
+def oracle_replicas(g: Group, dev=None, reps: int = 8, warmup: int = 1) -> dict:
     """The oracle on every host core this process may use: one replica process per core (spawned,
     never forked from a CUDA process), each running the single-threaded oracle over the k and v
     matrices of the layer on its own copy of the inputs (drawn once here and sent to each replica);
@@ -956,8 +957,8 @@ def cpu_baseline_all_cores(g: Group, dev=None, reps: int = 8) -> dict:
     nbytes = rs_bytes(sub, lay.S, lay.U) + ag_bytes(lay.U)
     ctx = mp.get_context("spawn")
     barrier, results = ctx.Barrier(n), ctx.Queue()
-    procs = [ctx.Process(target=_oracle_replica, args=(sub, grads, shards, reps, barrier, results), daemon=True)
-             for _ in range(n)]
+    procs = [ctx.Process(target=_oracle_replica, args=(sub, grads, shards, reps, warmup, barrier, results),
+                         daemon=True) for _ in range(n)]
     for p in procs:
         p.start()
     try:
@@ -975,35 +976,27 @@ def cpu_baseline_all_cores(g: Group, dev=None, reps: int = 8) -> dict:
             "cpu_model": cpu_model()}
 
 
-def run_reference(args):
-    """The reference arm: the CPU oracle, as it stands, timed on the host cores on a bounded
-    sample of the same workload, under the same metric."""
-    import oracle
+def cpu_baseline_all_cores(g: Group, dev=None, reps: int = 8) -> dict:
+    return oracle_replicas(g, dev, reps)
 
-    oracle.build()
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands (single-threaded C), timed on all the host
+    cores this process may use — one replica per core, each on its own copy of a bounded sample of
+    the same workload — under the same metric.  A step = one reduce-scatter + all-gather of the
+    sample on every replica."""
     g = workload(args)
-    sub = cpu_sample(g)
-    lay = oracle.plan(sub.R, sub.rows, sub.row_len)
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
-    grads, shards = cpu_inputs(sub, lay.S, dev)
-    params = [np.empty(sub.numel(p), np.uint16) for p in range(sub.P)]
-    nbytes = rs_bytes(sub, lay.S, lay.U) + ag_bytes(lay.U)
-    for _ in range(args.warmup):
-        oracle_step(oracle, lay, grads, shards, params)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle_step(oracle, lay, grads, shards, params)
-    dt = time.perf_counter() - t0
-    value = nbytes * args.steps / dt / 1e9
-    sample = (f"{g.name} restricted to {', '.join(p[0] for p in sub.params)}; each step = reduce-scatter + "
-              f"all-gather of that sample, single-threaded C oracle")
+    res = oracle_replicas(g, dev, reps=args.steps, warmup=args.warmup)
+    value = res["value"]
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic (same generator and workload shapes)",
-        "config": {"workload": g.name, "R": g.R, "P": g.P, "sample_params": [p[0] for p in sub.params],
-                   "step": "reduce_scatter + all_gather on the host oracle"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "warmup": args.warmup, "ms_per_step": res["seconds"] * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (same generator and workload shapes)",
+        "config": {"workload": g.name, "R": g.R, "P": g.P, "sample_params": ["k", "v"],
+                   "step": "reduce_scatter + all_gather on the host oracle, one replica per core"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": res["cores"], "kind": "oracle",
+                         "sample": res["sample"], "cpu_model": res["cpu_model"]},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
