@@ -848,25 +848,32 @@ def end_to_end(G, g, buf, S, U, dev, args, world):
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    state["computed"] = state["copied_out"] = None
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_c)
-    for k in range(n_in):
-        s_in[k].wait_event(e0)
-    for _ in range(steps):
-        step()
-    s_c.wait_stream(s_out)
-    e1.record(s_c)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    # three timed windows of `steps` steps; the median window is reported (the host link is shared
+    # with the machine's other tenants, and single windows varied by up to 1.8x)
+    windows = []
+    for _ in range(3):
+        state["computed"] = state["copied_out"] = None
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s_c)
+        for k in range(n_in):
+            s_in[k].wait_event(e0)
+        for _ in range(steps):
+            step()
+        s_c.wait_stream(s_out)
+        e1.record(s_c)
+        torch.cuda.synchronize()
+        windows.append(max_over_ranks(e0.elapsed_time(e1), world, dev))
+    ms = sorted(windows)[1]
     value = whole_job_gbs(rs_bytes(g, S, U) + ag_bytes(U), steps, world, ms)
     link = {"h2d_gbs_inputs_only": one_direction("h2d"), "d2h_gbs_same_bytes": one_direction("d2h")}
     del h_grads, h_ag, h_shards, h_params
     return {"value": value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": ms / steps, "host_link": link,
+            "windows_gbs": [whole_job_gbs(rs_bytes(g, S, U) + ag_bytes(U), steps, world, w) for w in windows],
             "how": "pinned host -> device copies of all inputs (4 streams), tide_reduce_scatter + "
                    "tide_all_gather, device -> pinned host copies of all outputs, every step; step k+1's "
-                   "input copies overlap step k's output copies"}
+                   "input copies overlap step k's output copies; median of 3 windows"}
 
 
 # ---- the host oracle ---------------------------------------------------------------------------
