@@ -639,6 +639,28 @@ def cta_sweep(G, buf, stream, args, concurrent):
     G.set_ctas(args.rs_ctas, args.ag_ctas)
     G.set_rs_variant(tide.TIDE_RS_AUTO)
     G.set_ag_variant(tide.TIDE_AG_AUTO)
+    # copy-engine placement: no SM is taken, so the only knob is how many copies run at once
+    # (the streams they are spread over); HBM and L2 contention is what slows the GEMM
+    G2 = tide.Group(G.R, list(zip(G.rows, G.row_len)), tide.TIDE_FLAG_CE_2D)
+    for form, grp in (("1d", G), ("2d", G2)):
+        for lanes in (1, 2, 4, 8):
+            grp.set_ce_lanes(lanes)
+            launch = lambda: [grp.all_gather_ce(buf.ag_list, buf.params, stream) for _ in range(8)]
+            with torch.cuda.stream(stream):
+                launch()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                launch()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1)
+            c = concurrent(launch, "ce", reps=2)
+            rows.append({"kind": "all_gather_ce", "variant": form, "ce_lanes": lanes, "ctas": 0,
+                         "alone_ms": ms / 8, "gbs": g_ag * 8 / (ms * 1e-3) / 1e9,
+                         "gemm_slowdown_pct": c["slowdown_pct"], "victim_rate": c["victim_rate"],
+                         "gemms": c["gemms_started_inside"]})
+    G.set_ce_lanes(args.ce_lanes or 8)
+    G2.close()
     return rows
 
 
