@@ -600,6 +600,11 @@ def interference(G, buf, stream, dev, args):
         lambda: [G.all_gather(buf.ag_list, buf.params, stream) for _ in range(8)], "ag"))
     out["all_gather_ce"] = dict(ctas=0, **concurrent(
         lambda: [G.all_gather_ce(buf.ag_list, buf.params, stream) for _ in range(8)], "ce"))
+    # the same copies over a single stream: fewer in flight, much less HBM/L2 contention
+    G.set_ce_lanes(1)
+    out["all_gather_ce_lanes1"] = dict(ctas=0, ce_lanes=1, **concurrent(
+        lambda: [G.all_gather_ce(buf.ag_list, buf.params, stream) for _ in range(8)], "ce"))
+    G.set_ce_lanes(args.ce_lanes or 8)
     return out
 
 
@@ -743,18 +748,30 @@ def probes(G, buf, stream, dev, args):
                       if inside else None})
     out["spin_curve"] = curve
 
-    # Table 4 / Table 5 for several reduce-scatter configurations
-    configs = [("bulk", 0), ("bulk", 16), ("bulk", 4), ("register", 16)]
+    # Table 4 / Table 5 for several reduce-scatter configurations, and for the copy-engine
+    # placement (8 placements back to back, so the victims and probes overlap it)
+    configs = [("reduce_scatter", "bulk", 0), ("reduce_scatter", "bulk", 16), ("reduce_scatter", "bulk", 4),
+               ("reduce_scatter", "register", 16), ("all_gather_ce", "1d", 1), ("all_gather_ce", "1d", 8),
+               ("all_gather_ce", "2d", 1)]
+    G2 = tide.Group(G.R, list(zip(G.rows, G.row_len)), tide.TIDE_FLAG_CE_2D)
     rows = []
     recs = torch.zeros(3 * sms, dtype=torch.int64, device=dev)
-    for variant, ctas in configs:
-        G.set_ctas(ctas, 0)
-        G.set_rs_variant(tide.TIDE_RS_BULK if variant == "bulk" else tide.TIDE_RS_REGISTER)
-        rs = lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream)
-        row = {"variant": variant, "ctas": ctas or G.get_ctas()[0]}
+    for coll, variant, n_ in configs:
+        if coll == "reduce_scatter":
+            G.set_ctas(n_, 0)
+            G.set_rs_variant(tide.TIDE_RS_BULK if variant == "bulk" else tide.TIDE_RS_REGISTER)
+            rs = lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream)
+            row = {"collective": coll, "variant": variant, "ctas": n_ or G.get_ctas()[0]}
+        else:
+            grp = G if variant == "1d" else G2
+            grp.set_ce_lanes(n_)
+            rs = lambda: [grp.all_gather_ce(buf.ag_list, buf.params, stream) for _ in range(8)]
+            row = {"collective": coll, "variant": variant, "ctas": 0, "ce_lanes": n_}
         for name, fn in victims.items():
             ms, inside = _window_times(rs, vs, fn, 48, stream)
-            row["rs_ms"] = ms
+            row["coll_ms"] = ms
+            if coll == "reduce_scatter":
+                row["rs_ms"] = ms
             row[name] = 100 * (statistics.median(inside) / t_alone[name] - 1) if inside else None
         # SM-id probes: 32 four-CTA clusters (the GEMM's shape) and one CTA per SM, 50 us each,
         # launched repeatedly while the reduce-scatter runs
@@ -787,6 +804,8 @@ def probes(G, buf, stream, dev, args):
         rows.append(row)
     G.set_ctas(args.rs_ctas, args.ag_ctas)
     G.set_rs_variant(tide.TIDE_RS_AUTO)
+    G.set_ce_lanes(args.ce_lanes or 8)
+    G2.close()
     out["table4_table5"] = rows
     del a2, b2, c2, x, y, z
     torch.cuda.empty_cache()
