@@ -18,6 +18,7 @@
 // %globaltimer and reports through *status, as in the reduce-scatter kernels.
 #include <algorithm>
 
+#include "copy_any.cuh"
 #include "tide_internal.h"
 
 namespace tide {
@@ -122,8 +123,7 @@ all_gather_bulk_kernel(const AgSeg* __restrict__ segs, int nsegs, int64_t nchunk
         int cur = 0;
         for (int64_t c = c_begin; c < c_end; ++c) {
             const Chunk k = chunk_of(segs, nsegs, cur, c, shards, params);
-            if (k.nb == 0)
-                for (int64_t e = t; e < k.n; e += nt) k.dst[e] = k.src[e];
+            if (k.nb == 0) copy_bf16_any_alignment<4>(k.dst, k.src, k.n, t, nt);
         }
         return;
     }

@@ -6,11 +6,13 @@
 // This kernel is the SM form of that placement: for every (source rank r, parameter p) the
 // planner emits the run of valid elements, shard_r[o_p, o_p + v(r,p)*L_p) -> param_p[r*s_p, ...),
 // cut into chunks of kAgChunk elements; CTAs walk the chunk list with a grid stride.  Each
-// thread moves kAgUnroll 16-byte vectors per chunk (all loads first, then all stores).  Padding
+// thread moves kAgUnroll 16-byte vectors per chunk (all loads first, then all stores); runs whose
+// offsets are not 16-byte aligned take the widest vectors their alignment allows.  Padding
 // is never read and nothing outside the parameters is written.  Roofline: HBM, 2 bytes read +
 // 2 bytes written per valid element.
 #include <algorithm>
 
+#include "copy_any.cuh"
 #include "tide_internal.h"
 
 namespace tide {
@@ -49,7 +51,7 @@ __device__ __forceinline__ int find_run(const AgSeg* __restrict__ segs, int nseg
     return lo;
 }
 
-__global__ void __launch_bounds__(kAgThreads)
+__global__ void __launch_bounds__(kAgThreads, kAgCtasPerSm)
 all_gather_kernel(const AgSeg* __restrict__ segs, int nsegs, int64_t nchunks,
                   const uint16_t* const* __restrict__ shards, uint16_t* const* __restrict__ params,
                   int allow_vec) {
@@ -78,7 +80,7 @@ all_gather_kernel(const AgSeg* __restrict__ segs, int nsegs, int64_t nchunks,
                 }
             }
         } else {
-            for (int64_t k = threadIdx.x; k < n; k += kAgThreads) dst[k] = src[k];
+            copy_bf16_any_alignment<kAgUnroll>(dst, src, n, threadIdx.x, kAgThreads);
         }
     }
 }

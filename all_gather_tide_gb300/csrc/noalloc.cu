@@ -92,7 +92,8 @@ extern "C" int tide_reduce_scatter_noalloc(int32_t R, int32_t P, const int64_t* 
     e = cudaMemcpyAsync(scratch, staging.data(), need, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return tide::record_cuda_error(e);
     unsigned char* base = static_cast<unsigned char*>(scratch);
-    e = tide::launch_reduce_scatter(reinterpret_cast<const tide::RsSeg*>(base), int(pl.rs.size()), pl.rs_chunks,
+    e = tide::launch_reduce_scatter(reinterpret_cast<const tide::RsSeg*>(base), int(pl.rs.size()), nullptr,
+                                    pl.rs_chunks,
                                     reinterpret_cast<const uint16_t* const*>(base + seg_bytes),
                                     reinterpret_cast<float* const*>(base + seg_bytes + npieces * sizeof(void*)), R,
                                     P, aligned ? 1 : 0, sms * tide::kRsCtasPerSm, st);

@@ -57,6 +57,7 @@ void make_work_lists(Plan* pl) {
     // Reduce-scatter: destination-major, parameter order within a shard, so each CTA pass
     // writes a contiguous run of the shard and reads R contiguous runs of gradient p.
     pl->rs.clear();
+    pl->rs_piece.clear();
     int64_t chunks = 0;
     for (int32_t d = 0; d < pl->R; ++d) {
         for (int32_t p = 0; p < pl->P; ++p) {
@@ -69,7 +70,9 @@ void make_work_lists(Plan* pl) {
             sg.d = d;
             sg.p = p;
             sg.vec = (sg.src_off % 8 == 0) && (sg.dst_off % 4 == 0);
-            chunks += (sg.total + kRsChunk - 1) / kRsChunk;
+            const int64_t n = (sg.total + kRsChunk - 1) / kRsChunk;
+            chunks += n;
+            pl->rs_piece.insert(pl->rs_piece.end(), size_t(n), int32_t(pl->rs.size()));
             pl->rs.push_back(sg);
         }
     }
@@ -110,8 +113,10 @@ void make_work_lists(Plan* pl) {
     pl->ag_chunks = chunks;
 
     pl->ag_bulk.clear();
+    pl->ag_vec_elems = 0;
     chunks = 0;
     for (AgSeg sg : pl->ag) {
+        if (sg.vec) pl->ag_vec_elems += sg.len;
         sg.chunk_begin = chunks;
         chunks += (sg.len + kAgBulkChunk - 1) / kAgBulkChunk;
         pl->ag_bulk.push_back(sg);

@@ -87,13 +87,16 @@ __device__ __forceinline__ int find_piece(const RsSeg* __restrict__ segs, int ns
 }
 
 __global__ void __launch_bounds__(kRsThreads, kRsCtasPerSm)
-reduce_scatter_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nchunks,
-                      const uint16_t* const* __restrict__ grads, float* const* __restrict__ shards,
+reduce_scatter_kernel(const RsSeg* __restrict__ segs, int nsegs, const int32_t* __restrict__ chunk_piece,
+                      int64_t nchunks, const uint16_t* const* __restrict__ grads, float* const* __restrict__ shards,
                       int R, int P, int allow_vec) {
     constexpr int kBatch = 8;  // ranks whose loads are in flight together
     int cur = 0;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        cur = find_piece(segs, nsegs, cur, c);
+        // the chunk's piece: from the planner's chunk -> piece table when there is one (one load
+        // instead of a search: a CTA's chunks are a grid stride apart, many pieces apart when the
+        // pieces are small), else by searching forward from the previous piece
+        cur = chunk_piece ? __ldg(&chunk_piece[c]) : find_piece(segs, nsegs, cur, c);
         const RsSeg sg = segs[cur];
         const int64_t base = (c - sg.chunk_begin) * kRsChunk;
         const int64_t n = min(kRsChunk, sg.total - base);                 // elements in this chunk
@@ -154,12 +157,13 @@ reduce_scatter_kernel(const RsSeg* __restrict__ segs, int nsegs, int64_t nchunks
 
 }  // namespace
 
-cudaError_t launch_reduce_scatter(const RsSeg* segs, int nsegs, int64_t nchunks,
+cudaError_t launch_reduce_scatter(const RsSeg* segs, int nsegs, const int32_t* chunk_piece, int64_t nchunks,
                                   const uint16_t* const* grads, float* const* shards, int R, int P,
                                   int allow_vec, int ctas, cudaStream_t stream) {
     if (nchunks <= 0) return cudaSuccess;
     const int grid = int(std::min<int64_t>(ctas, nchunks));
-    reduce_scatter_kernel<<<grid, kRsThreads, 0, stream>>>(segs, nsegs, nchunks, grads, shards, R, P, allow_vec);
+    reduce_scatter_kernel<<<grid, kRsThreads, 0, stream>>>(segs, nsegs, chunk_piece, nchunks, grads, shards, R, P,
+                                                          allow_vec);
     return cudaGetLastError();
 }
 

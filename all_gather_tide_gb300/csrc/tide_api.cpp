@@ -57,6 +57,7 @@ struct tide_group {
     uint32_t debug = 0;
     int* d_status = nullptr;  // device status word written by bounded waits that expire
     tide::RsSeg* d_rs = nullptr;
+    int32_t* d_rs_piece = nullptr;  // piece index of every register-path chunk
     tide::RsSeg* d_rs_bulk = nullptr;
     int32_t* d_rs_bulk_piece = nullptr;  // piece index of every bulk chunk
     tide::AgSeg* d_ag_bulk = nullptr;
@@ -96,6 +97,7 @@ void release(tide_group* g) {
     }
     if (g->fork) cudaEventDestroy(g->fork);
     if (g->d_rs) cudaFree(g->d_rs);
+    if (g->d_rs_piece) cudaFree(g->d_rs_piece);
     if (g->d_rs_bulk) cudaFree(g->d_rs_bulk);
     if (g->d_rs_bulk_piece) cudaFree(g->d_rs_bulk_piece);
     if (g->d_ag_bulk) cudaFree(g->d_ag_bulk);
@@ -196,6 +198,16 @@ struct CeLanes {
 
 int default_ctas(const tide_group* g, int per_sm) { return std::max(1, g->sm_count * per_sm); }
 
+// The bulk-copy placement needs 16-byte aligned pointers and moves only runs whose offsets are
+// 16-byte compatible (the rest go through three warps per CTA).  TIDE_AG_AUTO takes it when at
+// least 90 % of the elements can ride bulk copies, else the register path, whose CTAs copy every run
+// with the widest vectors its alignment allows.
+bool ag_uses_bulk(const tide_group* g, bool aligned) {
+    if (!aligned || !g->d_ag_bulk || g->ag_variant == TIDE_AG_REGISTER) return false;
+    if (g->ag_variant == TIDE_AG_BULK) return true;
+    return g->plan.ag_vec_elems * 10 >= g->plan.U * 9;
+}
+
 // Bulk-copy kernel unless the register path is asked for; it needs 16-byte aligned pointers (the
 // register path's element-wise fallback covers the rest).  Measured on GB300 it is the faster of
 // the two at every CTA count, most of all when the count is capped below the SM count.
@@ -269,6 +281,12 @@ int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* ro
     if (e == cudaSuccess) e = cudaMalloc(&g->d_ag, std::max<size_t>(1, ag.size()) * sizeof(tide::AgSeg));
     if (e == cudaSuccess && !rs.empty())
         e = cudaMemcpy(g->d_rs, rs.data(), rs.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
+    const auto& rsp = g->plan.rs_piece;
+    if (e == cudaSuccess && !rsp.empty()) {
+        e = cudaMalloc(&g->d_rs_piece, rsp.size() * sizeof(int32_t));
+        if (e == cudaSuccess)
+            e = cudaMemcpy(g->d_rs_piece, rsp.data(), rsp.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+    }
     if (e == cudaSuccess && !ag.empty())
         e = cudaMemcpy(g->d_ag, ag.data(), ag.size() * sizeof(tide::AgSeg), cudaMemcpyHostToDevice);
     const auto& rb = g->plan.rs_bulk;
@@ -350,8 +368,7 @@ int tide_group_get_ctas(tide_group_t g, int32_t* rs_ctas, int32_t* ag_ctas) {
     *rs_ctas = g->rs_ctas ? g->rs_ctas
                           : (g->rs_variant == TIDE_RS_REGISTER ? default_ctas(g, tide::kRsCtasPerSm) : g->sm_count);
     *ag_ctas = g->ag_ctas ? g->ag_ctas
-                          : default_ctas(g, g->ag_variant == TIDE_AG_REGISTER ? tide::kAgCtasPerSm
-                                                                              : tide::kAgBulkCtasPerSm);
+                          : default_ctas(g, ag_uses_bulk(g, true) ? tide::kAgBulkCtasPerSm : tide::kAgCtasPerSm);
     return TIDE_OK;
 }
 
@@ -388,8 +405,8 @@ int tide_reduce_scatter(tide_group_t g, const void* const* grads, void* const* s
                                              (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
     } else {
         const int ctas = g->rs_ctas ? g->rs_ctas : default_ctas(g, tide::kRsCtasPerSm);
-        e = tide::launch_reduce_scatter(g->d_rs, int(g->plan.rs.size()), g->plan.rs_chunks, gp, sp, R, P,
-                                        aligned ? 1 : 0, ctas, st);
+        e = tide::launch_reduce_scatter(g->d_rs, int(g->plan.rs.size()), g->d_rs_piece, g->plan.rs_chunks, gp, sp,
+                                        R, P, aligned ? 1 : 0, ctas, st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return finish_slot(g, k, st);
@@ -421,7 +438,7 @@ int tide_all_gather(tide_group_t g, const void* const* shards, void* const* para
     const auto* sp = reinterpret_cast<const uint16_t* const*>(dev);
     auto* pp = reinterpret_cast<uint16_t* const*>(dev + R);
     cudaError_t e;
-    if (aligned && g->d_ag_bulk && g->ag_variant != TIDE_AG_REGISTER) {
+    if (ag_uses_bulk(g, aligned)) {
         const int ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgBulkCtasPerSm);
         e = tide::launch_all_gather_bulk(g->d_ag_bulk, int(g->plan.ag_bulk.size()), g->plan.ag_bulk_chunks, sp, pp,
                                          ctas, g->d_status, g->timeout_ns, st);

@@ -72,6 +72,7 @@ struct Plan {
     int64_t S = 0, U = 0;
     std::vector<RsSeg> rs;
     int64_t rs_chunks = 0;
+    std::vector<int32_t> rs_piece;  // index in rs of every chunk's piece
     std::vector<RsSeg> rs_bulk;  // same pieces, chunked for the bulk-copy kernel
     int64_t rs_bulk_chunks = 0;
     std::vector<int32_t> rs_bulk_piece;  // index in rs_bulk of every bulk chunk's piece
@@ -79,6 +80,7 @@ struct Plan {
     int64_t ag_chunks = 0;
     std::vector<AgSeg> ag_bulk;  // same runs, chunked for the bulk-copy placement kernel
     int64_t ag_bulk_chunks = 0;
+    int64_t ag_vec_elems = 0;  // valid elements in runs whose offsets allow 16-byte vectors
 };
 
 // Returns 0 or a negative TIDE_* status.
@@ -90,7 +92,8 @@ int64_t valid_rows(int64_t rows_p, int64_t m_p, int64_t d);
 int record_cuda_error(cudaError_t e);
 
 // Kernel launchers (stream-ordered; return the launch status).
-cudaError_t launch_reduce_scatter(const RsSeg* segs, int nsegs, int64_t nchunks,
+// chunk_piece: piece index of every chunk, or nullptr (the kernel then searches the piece list)
+cudaError_t launch_reduce_scatter(const RsSeg* segs, int nsegs, const int32_t* chunk_piece, int64_t nchunks,
                                   const uint16_t* const* grads, float* const* shards, int R, int P,
                                   int allow_vec, int ctas, cudaStream_t stream);
 // Bulk-copy variant: dynamic shared memory per CTA (stages + the current piece's R pointers), and

@@ -295,6 +295,35 @@ def test_all_gather_ce_2d_matches_oracle(tide, g):
     assert copies == expect
 
 
+def _shifted_groups():
+    """Groups whose small 1-D parameters shift every later prefix offset by 1, 2 or 4 elements, so
+    the placement meets every relative alignment of shard and parameter addresses (and a
+    Qwen3-shaped group at R = 64, where the per-rank norm pieces of 2 elements do this)."""
+    gs = []
+    for shift in (1, 2, 3, 4, 5, 7):
+        params = []
+        for i, (rows, l) in enumerate([(64, 96), (40, 128), (8 * shift, 1), (72, 40), (8 * shift, 1),
+                                       (33, 24), (256, 8), (8 * shift + 8, 1), (48, 64)]):
+            params.append((f"p{i}", rows, l))
+        gs.append(Group(f"shift{shift}", 8, tuple(params)))
+    q = group("qwen3moe").scaled(16)
+    gs.append(Group("qwen-scaled16-R64", 64, q.params))
+    return gs
+
+
+@pytest.mark.parametrize("variant", [0, 1, 2], ids=["auto", "register", "bulk"])
+@pytest.mark.parametrize("g", _shifted_groups(), ids=lambda g: g.name)
+def test_all_gather_any_relative_alignment(tide, g, variant):
+    run_ag(tide, g, variant=variant)
+    run_ag(tide, g, variant=variant, misalign=True)
+
+
+@pytest.mark.parametrize("g", _shifted_groups(), ids=lambda g: g.name)
+def test_reduce_scatter_any_relative_alignment(tide, g):
+    run_rs(tide, g)
+    run_rs(tide, g, variant=1)
+
+
 @pytest.mark.parametrize("ctas", [1, 3, 17, 152, 1000])
 def test_cta_count_does_not_change_bits(tide, ctas):
     run_rs(tide, group("qwen3moe").scaled(16), ctas=ctas)
