@@ -332,16 +332,27 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, const int32_t* __rest
                     phase ^= 1u;
                 }
             }
-            const bool wide = (reinterpret_cast<uintptr_t>(dst) & 31u) == 0;  // 32-byte stores possible
+            // the widest stores the destination allows: the shard offset o_p of a parameter placed
+            // after small 1-D parameters need not be a multiple of 4 elements
+            const unsigned da = unsigned(reinterpret_cast<uintptr_t>(dst) & 31u);
+            const int sw = da == 0 ? 32 : (da & 15u) == 0 ? 16 : (da & 7u) == 0 ? 8 : 4;  // bytes
 #pragma unroll
             for (int j = 0; j < kGroups; ++j) {
                 const int64_t e = (int64_t(j) * kConsumers + ctid) * 8;
                 if (whole || e + 8 <= v.nbulk) {
-                    if (wide) {
+                    const float* a = acc[j];
+                    if (sw == 32) {
                         st_cs_v8(dst + e, acc[j]);
+                    } else if (sw == 16) {
+                        __stcs(reinterpret_cast<float4*>(dst + e), make_float4(a[0], a[1], a[2], a[3]));
+                        __stcs(reinterpret_cast<float4*>(dst + e + 4), make_float4(a[4], a[5], a[6], a[7]));
+                    } else if (sw == 8) {
+#pragma unroll
+                        for (int k = 0; k < 8; k += 2)
+                            __stcs(reinterpret_cast<float2*>(dst + e + k), make_float2(a[k], a[k + 1]));
                     } else {
-                        __stcs(reinterpret_cast<float4*>(dst + e), make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]));
-                        __stcs(reinterpret_cast<float4*>(dst + e + 4), make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]));
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) __stcs(dst + e + k, a[k]);
                     }
                 }
             }
