@@ -66,14 +66,13 @@ extern "C" int tide_reduce_scatter_noalloc(int32_t R, int32_t P, const int64_t* 
     std::vector<unsigned char> staging(need);
     const void** table = reinterpret_cast<const void**>(staging.data() + seg_bytes);
     for (size_t i = 0; i < npieces; ++i) {
-        if (!grads[i]) return TIDE_EINVAL;
+        if (!grads[i] || (reinterpret_cast<uintptr_t>(grads[i]) & 1u)) return TIDE_EINVAL;
         table[i] = grads[i];
         aligned &= (reinterpret_cast<uintptr_t>(grads[i]) & 15u) == 0;
     }
     for (int d = 0; d < R; ++d) {
-        if (!shards[d]) return TIDE_EINVAL;
-        table[npieces + d] = shards[d];
-        aligned &= (reinterpret_cast<uintptr_t>(shards[d]) & 15u) == 0;
+        if (!shards[d] || (reinterpret_cast<uintptr_t>(shards[d]) & 3u)) return TIDE_EINVAL;
+        table[npieces + d] = shards[d];  // any fp32 alignment: the kernel picks its store width
     }
     std::copy(reinterpret_cast<const unsigned char*>(pl.rs.data()),
               reinterpret_cast<const unsigned char*>(pl.rs.data() + pl.rs.size()), staging.begin());

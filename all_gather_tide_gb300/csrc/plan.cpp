@@ -69,7 +69,7 @@ void make_work_lists(Plan* pl) {
             sg.chunk_begin = chunks;
             sg.d = d;
             sg.p = p;
-            sg.vec = (sg.src_off % 8 == 0) && (sg.dst_off % 4 == 0);
+            sg.vec = sg.src_off % 8 == 0;  // 16-byte gradient loads; stores adapt to the shard offset
             const int64_t n = (sg.total + kRsChunk - 1) / kRsChunk;
             chunks += n;
             pl->rs_piece.insert(pl->rs_piece.end(), size_t(n), int32_t(pl->rs.size()));
@@ -84,7 +84,6 @@ void make_work_lists(Plan* pl) {
     chunks = 0;
     for (RsSeg sg : pl->rs) {
         sg.chunk_begin = chunks;
-        sg.vec = sg.src_off % 8 == 0;  // bulk copies need only the gradient side aligned
         const int64_t n = (sg.total + kBulkChunk - 1) / kBulkChunk;
         chunks += n;
         pl->rs_bulk_piece.insert(pl->rs_bulk_piece.end(), size_t(n), int32_t(pl->rs_bulk.size()));

@@ -86,6 +86,20 @@ __device__ __forceinline__ int find_piece(const RsSeg* __restrict__ segs, int ns
     return lo;
 }
 
+// Stores 8 fp32 values with the widest stores `sw` (16, 8 or 4 bytes) allows.
+__device__ __forceinline__ void store8(float* p, const float (&a)[8], unsigned sw) {
+    if (sw == 16u) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(a[0], a[1], a[2], a[3]));
+        __stcs(reinterpret_cast<float4*>(p + 4), make_float4(a[4], a[5], a[6], a[7]));
+    } else if (sw == 8u) {
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) __stcs(reinterpret_cast<float2*>(p + k), make_float2(a[k], a[k + 1]));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) __stcs(p + k, a[k]);
+    }
+}
+
 __global__ void __launch_bounds__(kRsThreads, kRsCtasPerSm)
 reduce_scatter_kernel(const RsSeg* __restrict__ segs, int nsegs, const int32_t* __restrict__ chunk_piece,
                       int64_t nchunks, const uint16_t* const* __restrict__ grads, float* const* __restrict__ shards,
@@ -132,16 +146,17 @@ reduce_scatter_kernel(const RsSeg* __restrict__ segs, int nsegs, const int32_t* 
                     }
                 }
             }
+            // the widest stores the shard offset allows (o_p need not be a multiple of 4 elements)
+            const unsigned da = unsigned(reinterpret_cast<uintptr_t>(dst) & 15u);
+            const unsigned sw = da == 0 ? 16u : (da & 7u) == 0 ? 8u : 4u;
 #pragma unroll
             for (int u = 0; u < kRsUnroll; ++u) {
                 const int64_t e = (int64_t(u) * kRsThreads + threadIdx.x) * 8;
                 if (full[u]) {
-                    __stcs(reinterpret_cast<float4*>(dst + e), make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]));
-                    __stcs(reinterpret_cast<float4*>(dst + e + 4), make_float4(acc[u][4], acc[u][5], acc[u][6], acc[u][7]));
+                    store8(dst + e, acc[u], sw);
                 } else if (e >= nvalid && e + 8 <= n) {
-                    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-                    __stcs(reinterpret_cast<float4*>(dst + e), z);
-                    __stcs(reinterpret_cast<float4*>(dst + e + 4), z);
+                    const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                    store8(dst + e, z, sw);
                 } else if (e < n) {
                     // group straddling the end of the valid rows or of the piece
                     for (int k = 0; k < 8 && e + k < n; ++k)

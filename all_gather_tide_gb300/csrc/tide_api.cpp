@@ -154,6 +154,10 @@ int finish_slot(tide_group* g, int k, cudaStream_t stream) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// A pointer the kernels dereference element by element must be aligned to its element size
+// (2 bytes for bf16, 4 for fp32): anything else would be a misaligned access on the device.
+bool elem_aligned(const void* p, unsigned bytes) { return (reinterpret_cast<uintptr_t>(p) & (bytes - 1u)) == 0; }
+
 // Stream-ordered fan-out of copy-engine work: lane 0 is the caller's stream; lanes 1.. are helper
 // streams that start after everything already enqueued on the caller's stream and that the
 // caller's stream waits for at the end.
@@ -379,14 +383,15 @@ int tide_reduce_scatter(tide_group_t g, const void* const* grads, void* const* s
     std::vector<const void*> table(size_t(R) * P + R);
     bool aligned = true;
     for (size_t i = 0; i < size_t(R) * P; ++i) {
-        if (!grads[i]) return TIDE_EINVAL;
+        if (!grads[i] || !elem_aligned(grads[i], 2)) return TIDE_EINVAL;
         table[i] = grads[i];
         aligned &= aligned16(grads[i]);
     }
+    // the kernels store the sums with whatever vectors each shard address allows, so only the
+    // gradients' alignment decides between the vector paths and the element-wise one
     for (int d = 0; d < R; ++d) {
-        if (!shards[d]) return TIDE_EINVAL;
+        if (!shards[d] || !elem_aligned(shards[d], 4)) return TIDE_EINVAL;
         table[size_t(R) * P + d] = shards[d];
-        aligned &= aligned16(shards[d]);
     }
     if (!aligned && (g->flags & TIDE_FLAG_VEC_STRICT)) return TIDE_EALIGN;
     int rc = check_device(g);
@@ -419,12 +424,12 @@ int tide_all_gather(tide_group_t g, const void* const* shards, void* const* para
     std::vector<const void*> table(size_t(R) + P);
     bool aligned = true;
     for (int r = 0; r < R; ++r) {
-        if (!shards[r]) return TIDE_EINVAL;
+        if (!shards[r] || !elem_aligned(shards[r], 2)) return TIDE_EINVAL;
         table[r] = shards[r];
         aligned &= aligned16(shards[r]);
     }
     for (int p = 0; p < P; ++p) {
-        if (!params[p]) return TIDE_EINVAL;
+        if (!params[p] || !elem_aligned(params[p], 2)) return TIDE_EINVAL;
         table[size_t(R) + p] = params[p];
         aligned &= aligned16(params[p]);
     }

@@ -48,8 +48,8 @@ struct RsSeg {
     int64_t total;        // s_p
     int64_t chunk_begin;  // index of the piece's first chunk in the flat chunk list
     int32_t d, p;
-    int32_t vec;  // register-path list: both offsets allow 16-byte vectors (src_off % 8 == 0,
-                  // dst_off % 4 == 0); bulk list: the gradient offset allows bulk copies (src_off % 8 == 0)
+    int32_t vec;  // the gradient offset allows 16-byte loads and bulk copies (src_off % 8 == 0); the
+                  // kernels store with the widest vectors the shard offset allows
     int32_t pad_;
 };
 static_assert(sizeof(RsSeg) == 56, "RsSeg layout");

@@ -43,8 +43,10 @@ extern "C" {
 
 /* ---- status codes ------------------------------------------------------------------------ */
 #define TIDE_OK 0
-#define TIDE_EINVAL (-1)  /* null pointer, R < 1, P < 1, rows < 1, row_len < 1, bad index, wrong device */
-#define TIDE_EALIGN (-2)  /* TIDE_FLAG_VEC_STRICT set and a pointer is not 16-byte aligned */
+#define TIDE_EINVAL (-1)  /* null pointer, R < 1, P < 1, rows < 1, row_len < 1, bad index, wrong device,
+                            or a device pointer not aligned to its element (2 bytes bf16, 4 bytes fp32) */
+#define TIDE_EALIGN (-2)  /* TIDE_FLAG_VEC_STRICT set and a pointer that needs 16-byte alignment lacks it
+                            (reduce-scatter: a gradient; placement: a shard or a parameter) */
 #define TIDE_ELAYOUT (-3) /* TIDE_FLAG_CE_STRICT set and the shards are not at a uniform pitch */
 #define TIDE_ECUDA (-4)   /* a CUDA runtime call failed; tide_last_cuda_error() gives its code */
 #define TIDE_ENOMEM (-5)  /* host or device allocation of the group's own tables failed */
@@ -122,8 +124,11 @@ int tide_group_get_ctas(tide_group_t g, int32_t *rs_ctas, int32_t *ag_ctas);
  *   grads:  host array of R*P device pointers, entry [r*P + p] = rank r's bf16 gradient of p
  *           (rows_p*L_p elements, row-major, contiguous).  Read only, never packed.
  *   shards: host array of R device pointers, entry d = rank d's fp32 shard of S elements.
- * 16-byte aligned pointers take the vectorised path; others take an element-wise path with the
- * same results (or TIDE_EALIGN under TIDE_FLAG_VEC_STRICT).
+ * With 16-byte aligned gradient pointers the gradients are read with 16-byte loads or bulk copies
+ * (pieces whose offset d*s_p is a multiple of 8 elements) and the sums are stored with the widest
+ * vectors each shard address allows (shards need only fp32 alignment); gradient pointers that are
+ * not 16-byte aligned take an element-wise path with the same results (or TIDE_EALIGN under
+ * TIDE_FLAG_VEC_STRICT).
  */
 int tide_reduce_scatter(tide_group_t g, const void *const *grads, void *const *shards,
                         void *stream);

@@ -594,3 +594,45 @@ def test_ce_lanes_stay_stream_ordered(tide, lanes, flags):
     for p in range(g.P):
         assert np.array_equal(outs[p].cpu().numpy().view(np.uint16), want[p]), (lanes, p)
     G.close()
+
+
+def test_element_misaligned_pointers_are_rejected(tide):
+    """Pointers that are not aligned to their element size are refused before anything runs."""
+    g = group("tiny")
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+    raw = torch.zeros(1 << 12, dtype=torch.uint8, device="cuda")
+    odd = raw.data_ptr() + 1   # not 2-byte aligned
+    two = raw.data_ptr() + 2   # 2-byte but not 4-byte aligned
+    good16 = raw.data_ptr()
+    grads = [[good16] * g.P for _ in range(g.R)]
+    for bad_g, bad_s in ((odd, good16), (good16, two)):
+        gp = [[bad_g if (r, p) == (1, 1) else good16 for p in range(g.P)] for r in range(g.R)]
+        sp = [bad_s if d == 2 else good16 for d in range(g.R)]
+        with pytest.raises(tide.TideError) as e:
+            G.reduce_scatter(gp, sp)
+        assert e.value.status == tide.TIDE_EINVAL
+    with pytest.raises(tide.TideError) as e:
+        G.all_gather([good16] * g.R, [odd] + [good16] * (g.P - 1))
+    assert e.value.status == tide.TIDE_EINVAL
+    torch.cuda.synchronize()
+    G.close()
+
+
+def test_shards_need_only_fp32_alignment(tide):
+    """Shard pointers 4 or 8 bytes past a 16-byte boundary keep the vector paths (same bits)."""
+    g = group("llama8b").scaled(32)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    host = rng.group_grads(g)
+    want = oracle.reduce_scatter(lay, [[t.numpy().view(np.uint16) for t in row] for row in host])
+    grads = [[t.cuda() for t in row] for row in host]
+    for off in (1, 2, 3):
+        buf = torch.full((g.R, lay.S + 4), float("nan"), device="cuda")
+        shards = [buf[d, off:off + lay.S] for d in range(g.R)]
+        for variant in (tide.TIDE_RS_BULK, tide.TIDE_RS_REGISTER):
+            G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+            G.set_rs_variant(variant)
+            G.reduce_scatter(grads, shards)
+            torch.cuda.synchronize()
+            for d in range(g.R):
+                assert np.array_equal(f32_bits(shards[d]), want[d].view(np.uint32)), (off, variant, d)
+            G.close()
