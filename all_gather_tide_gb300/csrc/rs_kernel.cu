@@ -2,8 +2,8 @@
 //
 // Paper: "The Endgame of FSDP Communication" (arXiv 2610.38228).  The paper's reduce-scatter
 // takes each parameter's bf16 gradient where it lies (Table 1, the in-place read row: no
-// full-group pack) and sums into fp32 shards (abstract); Fig. 2b step 5 forms the fp32 sums with a bounded number of
-// short-lived CTAs.  On one GPU every contributor rank is a buffer in local HBM, so the sum CTAs
+// full-group pack) and sums into fp32 shards (abstract); Fig. 2b step 5 forms the fp32 sums with
+// a bounded number of short-lived CTAs.  On one GPU every contributor rank is a buffer in local HBM, so the sum CTAs
 // read the R gradients directly, and the landing step is folded into the same pass: each fp32
 // result is stored once, at its final address in the destination shard (Fig. 1).
 //
@@ -13,7 +13,10 @@
 // elements: it issues the 16-byte bf16 loads of up to 8 ranks x kRsUnroll groups back to back
 // (memory-level parallelism), widens them exactly (bf16 bits << 16), adds them into fp32 in
 // ascending rank order starting from rank 0's value, and writes two 16-byte fp32 stores per
-// group.  Padding elements of the piece are written as +0.0f without any load.
+// group (8- or 4-byte stores when the shard offset of the piece is less aligned).  Padding
+// elements of the piece are written as +0.0f without any load.  Pieces whose gradient offset
+// d*s_p is not a multiple of 8 elements, or gradient pointers that are not 16-byte aligned, take
+// an element-wise path.
 //
 // The data are streamed once: loads bypass L1 (ld.global.nc.L1::no_allocate) and stores are
 // marked evict-first (st.global.cs).  Roofline: HBM, R*2 bytes read + 4 bytes written per valid

@@ -212,8 +212,8 @@ bool ag_uses_bulk(const tide_group* g, bool aligned) {
     return g->plan.ag_vec_elems * 10 >= g->plan.U * 9;
 }
 
-// Bulk-copy kernel unless the register path is asked for; it needs 16-byte aligned pointers (the
-// register path's element-wise fallback covers the rest).  Measured on GB300 it is the faster of
+// Bulk-copy kernel unless the register path is asked for; it needs 16-byte aligned gradient
+// pointers (the register path's element-wise fallback covers the rest).  Measured on GB300 it is the faster of
 // the two at every CTA count, most of all when the count is capped below the SM count.
 bool use_bulk(const tide_group* g, bool aligned) {
     if (!aligned || g->plan.rs_bulk.empty() || !g->d_rs_bulk || !g->d_rs_bulk_piece) return false;

@@ -56,8 +56,9 @@ extern "C" {
 #define TIDE_MAX_TABLE (1 << 22) /* max R*P pointer-table entries */
 
 /* ---- group flags ------------------------------------------------------------------------- */
-/* Return TIDE_EALIGN instead of running the element-wise path when a pointer passed to
- * tide_reduce_scatter / tide_all_gather is not 16-byte aligned. */
+/* Return TIDE_EALIGN instead of running the element-wise path when a pointer whose 16-byte
+ * alignment the vector paths need is not 16-byte aligned: a gradient for tide_reduce_scatter, a
+ * shard or a parameter for tide_all_gather. */
 #define TIDE_FLAG_VEC_STRICT 0x1u
 /* With TIDE_FLAG_CE_2D: return TIDE_ELAYOUT from tide_all_gather_ce instead of falling back to
  * 1-D copies when shards[r] != shards[0] + r*pitch for one pitch >= S*2 bytes. */
