@@ -52,12 +52,14 @@ __device__ __forceinline__ int find_run(const AgSeg* __restrict__ segs, int nseg
 }
 
 __global__ void __launch_bounds__(kAgThreads, kAgCtasPerSm)
-all_gather_kernel(const AgSeg* __restrict__ segs, int nsegs, int64_t nchunks,
+all_gather_kernel(const AgSeg* __restrict__ segs, int nsegs, const int32_t* __restrict__ chunk_run, int64_t nchunks,
                   const uint16_t* const* __restrict__ shards, uint16_t* const* __restrict__ params,
                   int allow_vec) {
     int cur = 0;
     for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
-        cur = find_run(segs, nsegs, cur, c);
+        // the chunk's run: one load from the planner's chunk -> run table (a CTA's chunks are a
+        // grid stride apart, many runs apart when runs are short), else a forward search
+        cur = chunk_run ? __ldg(&chunk_run[c]) : find_run(segs, nsegs, cur, c);
         const AgSeg sg = segs[cur];
         const int64_t base = (c - sg.chunk_begin) * kAgChunk;
         const int64_t n = min(kAgChunk, sg.len - base);
@@ -87,12 +89,12 @@ all_gather_kernel(const AgSeg* __restrict__ segs, int nsegs, int64_t nchunks,
 
 }  // namespace
 
-cudaError_t launch_all_gather(const AgSeg* segs, int nsegs, int64_t nchunks,
+cudaError_t launch_all_gather(const AgSeg* segs, int nsegs, const int32_t* chunk_run, int64_t nchunks,
                               const uint16_t* const* shards, uint16_t* const* params,
                               int allow_vec, int ctas, cudaStream_t stream) {
     if (nchunks <= 0) return cudaSuccess;
     const int grid = int(std::min<int64_t>(ctas, nchunks));
-    all_gather_kernel<<<grid, kAgThreads, 0, stream>>>(segs, nsegs, nchunks, shards, params, allow_vec);
+    all_gather_kernel<<<grid, kAgThreads, 0, stream>>>(segs, nsegs, chunk_run, nchunks, shards, params, allow_vec);
     return cudaGetLastError();
 }
 

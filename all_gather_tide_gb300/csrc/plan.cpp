@@ -93,6 +93,7 @@ void make_work_lists(Plan* pl) {
 
     // All-gather placement: source-rank-major runs of valid elements; padding never appears.
     pl->ag.clear();
+    pl->ag_run.clear();
     chunks = 0;
     for (int32_t r = 0; r < pl->R; ++r) {
         for (int32_t p = 0; p < pl->P; ++p) {
@@ -106,7 +107,9 @@ void make_work_lists(Plan* pl) {
             sg.r = r;
             sg.p = p;
             sg.vec = (sg.src_off % 8 == 0) && (sg.dst_off % 8 == 0);
-            chunks += (len + kAgChunk - 1) / kAgChunk;
+            const int64_t n = (len + kAgChunk - 1) / kAgChunk;
+            chunks += n;
+            pl->ag_run.insert(pl->ag_run.end(), size_t(n), int32_t(pl->ag.size()));
             pl->ag.push_back(sg);
         }
     }

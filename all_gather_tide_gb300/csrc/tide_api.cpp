@@ -62,6 +62,7 @@ struct tide_group {
     int32_t* d_rs_bulk_piece = nullptr;  // piece index of every bulk chunk
     tide::AgSeg* d_ag_bulk = nullptr;
     tide::AgSeg* d_ag = nullptr;
+    int32_t* d_ag_run = nullptr;  // run index of every register-path placement chunk
     size_t slot_cap = 0;
     Slot slots[kSlots];
     uint64_t use_clock = 0;
@@ -103,6 +104,7 @@ void release(tide_group* g) {
     if (g->d_ag_bulk) cudaFree(g->d_ag_bulk);
     if (g->d_status) cudaFree(g->d_status);
     if (g->d_ag) cudaFree(g->d_ag);
+    if (g->d_ag_run) cudaFree(g->d_ag_run);
     delete g;
 }
 
@@ -204,12 +206,18 @@ int default_ctas(const tide_group* g, int per_sm) { return std::max(1, g->sm_cou
 
 // The bulk-copy placement needs 16-byte aligned pointers and moves only runs whose offsets are
 // 16-byte compatible (the rest go through three warps per CTA).  TIDE_AG_AUTO takes it when at
-// least 90 % of the elements can ride bulk copies, else the register path, whose CTAs copy every run
-// with the widest vectors its alignment allows.
+// least 90 % of the elements can ride bulk copies and either the CTA count is capped below the SM
+// count (a bulk CTA moves far more per SM) or the runs are long (>= 1 M elements on average);
+// otherwise the register path, whose CTAs copy every run with the widest vectors its alignment
+// allows.  Measured on GB300 at the default grid: bulk 6.7-6.8 TB/s against register 6.5 on the
+// Llama-3.1-70B layer (12 M-element runs), register 6.7 against bulk 6.5 on the Qwen3 MoE layer
+// (0.2 M) and the Wan sweep at R = 64 (0.4 M).
 bool ag_uses_bulk(const tide_group* g, bool aligned) {
     if (!aligned || !g->d_ag_bulk || g->ag_variant == TIDE_AG_REGISTER) return false;
     if (g->ag_variant == TIDE_AG_BULK) return true;
-    return g->plan.ag_vec_elems * 10 >= g->plan.U * 9;
+    if (g->plan.ag_vec_elems * 10 < g->plan.U * 9) return false;
+    if (g->ag_ctas > 0 && g->ag_ctas < g->sm_count) return true;
+    return g->plan.ag.empty() || g->plan.U >= int64_t(g->plan.ag.size()) * (int64_t(1) << 20);
 }
 
 // Bulk-copy kernel unless the register path is asked for; it needs 16-byte aligned gradient
@@ -293,6 +301,12 @@ int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* ro
     }
     if (e == cudaSuccess && !ag.empty())
         e = cudaMemcpy(g->d_ag, ag.data(), ag.size() * sizeof(tide::AgSeg), cudaMemcpyHostToDevice);
+    const auto& agr = g->plan.ag_run;
+    if (e == cudaSuccess && !agr.empty()) {
+        e = cudaMalloc(&g->d_ag_run, agr.size() * sizeof(int32_t));
+        if (e == cudaSuccess)
+            e = cudaMemcpy(g->d_ag_run, agr.data(), agr.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+    }
     const auto& rb = g->plan.rs_bulk;
     if (e == cudaSuccess && !rb.empty()) {
         e = cudaMalloc(&g->d_rs_bulk, rb.size() * sizeof(tide::RsSeg));
@@ -449,8 +463,8 @@ int tide_all_gather(tide_group_t g, const void* const* shards, void* const* para
                                          ctas, g->d_status, g->timeout_ns, st);
     } else {
         const int ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgCtasPerSm);
-        e = tide::launch_all_gather(g->d_ag, int(g->plan.ag.size()), g->plan.ag_chunks, sp, pp, aligned ? 1 : 0, ctas,
-                                    st);
+        e = tide::launch_all_gather(g->d_ag, int(g->plan.ag.size()), g->d_ag_run, g->plan.ag_chunks, sp, pp,
+                                    aligned ? 1 : 0, ctas, st);
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return finish_slot(g, k, st);

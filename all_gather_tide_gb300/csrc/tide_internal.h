@@ -79,6 +79,7 @@ struct Plan {
     std::vector<int32_t> rs_bulk_piece;  // index in rs_bulk of every bulk chunk's piece
     std::vector<AgSeg> ag;
     int64_t ag_chunks = 0;
+    std::vector<int32_t> ag_run;  // index in ag of every chunk's run
     std::vector<AgSeg> ag_bulk;  // same runs, chunked for the bulk-copy placement kernel
     int64_t ag_bulk_chunks = 0;
     int64_t ag_vec_elems = 0;  // valid elements in runs whose offsets allow 16-byte vectors
@@ -109,7 +110,8 @@ size_t ag_bulk_smem_bytes();
 cudaError_t launch_all_gather_bulk(const AgSeg* segs, int nsegs, int64_t nchunks, const uint16_t* const* shards,
                                    uint16_t* const* params, int ctas, int* status, uint64_t timeout_ns,
                                    cudaStream_t stream);
-cudaError_t launch_all_gather(const AgSeg* segs, int nsegs, int64_t nchunks,
+// chunk_run: run index of every chunk, or nullptr (the kernel then searches the run list)
+cudaError_t launch_all_gather(const AgSeg* segs, int nsegs, const int32_t* chunk_run, int64_t nchunks,
                               const uint16_t* const* shards, uint16_t* const* params,
                               int allow_vec, int ctas, cudaStream_t stream);
 
