@@ -173,8 +173,10 @@ int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *p
  */
 int tide_group_set_rs_variant(tide_group_t g, int32_t variant);
 
-#define TIDE_AG_AUTO 0     /* bulk-copy placement when every pointer is 16-byte aligned and >= 90 % of the
-                              elements lie in runs with 16-byte compatible offsets, else register path */
+#define TIDE_AG_AUTO 0     /* bulk-copy placement when every pointer is 16-byte aligned, >= 90 % of the
+                              elements lie in runs with 16-byte compatible offsets, and either the CTA
+                              count is capped below the SM count or the runs average >= 1 M elements;
+                              else the register path */
 #define TIDE_AG_REGISTER 1 /* 16-byte register loads and stores (8, 4 or 2 bytes for runs whose offsets
                               allow no wider vectors), 4 CTAs per SM */
 #define TIDE_AG_BULK 2     /* 48 KB bulk copies in and out of shared memory driven by one thread per CTA */
