@@ -162,7 +162,7 @@ int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *p
                        void *stream);
 
 /* ---- reduce-scatter kernel variants and device-side waits --------------------------------- */
-#define TIDE_RS_AUTO 0     /* bulk-copy path when every pointer is 16-byte aligned, else register path */
+#define TIDE_RS_AUTO 0     /* bulk-copy path when every gradient pointer is 16-byte aligned, else register path */
 #define TIDE_RS_REGISTER 1 /* 16-byte register loads of 8 ranks in flight per thread, 2 CTAs per SM */
 #define TIDE_RS_BULK 2     /* 45 KB bulk asynchronous copies, one rank row per stage, 1 CTA per SM */
 
@@ -177,8 +177,9 @@ int tide_group_set_rs_variant(tide_group_t g, int32_t variant);
                               elements lie in runs with 16-byte compatible offsets, and either the CTA
                               count is capped below the SM count or the runs average >= 1 M elements;
                               else the register path */
-#define TIDE_AG_REGISTER 1 /* 16-byte register loads and stores (8, 4 or 2 bytes for runs whose offsets
-                              allow no wider vectors), 4 CTAs per SM */
+#define TIDE_AG_REGISTER 1 /* 16-byte register loads and stores (for runs whose shard and parameter
+                              addresses differ in 16-byte alignment, 16-byte stores assembled from two
+                              aligned loads each), 4 CTAs per SM */
 #define TIDE_AG_BULK 2     /* 48 KB bulk copies in and out of shared memory driven by one thread per CTA */
 
 /* Chooses the placement kernel of tide_all_gather; both write the same bits.  The bulk path needs

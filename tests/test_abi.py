@@ -119,3 +119,19 @@ def test_pointer_table_marshalling(tide):
     assert tide._ptr_array(t) is t and tide._flat_grads(t) is t
     L = tide.lib()
     assert L.tide_reduce_scatter(None, t, t, None) == tide.TIDE_EINVAL
+
+
+def test_header_constants_match_binding(tide):
+    """Every integer constant the header defines has the same value in the binding (where the binding
+    exposes it)."""
+    src = open(os.path.join(ROOT, "include", "tide.h")).read()
+    seen = 0
+    for name, value in re.findall(r"^#define\s+(TIDE_\w+)\s+([^/\n]+)", src, flags=re.M):
+        expr = value.strip().replace("u", "")
+        if not re.fullmatch(r"[-()0-9x<\s]+", expr):
+            continue
+        v = eval(expr)  # integer literals, shifts and parentheses only
+        if hasattr(tide, name):
+            assert getattr(tide, name) == v, name
+            seen += 1
+    assert seen >= 15
