@@ -61,6 +61,7 @@ SIGNATURES = {
     "tide_group_set_rs_variant": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "tide_group_set_ag_variant": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "tide_group_set_ce_lanes": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "tide_group_ag_kernel": (ctypes.c_int, [_vp, _i32p]),
     "tide_group_set_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_uint64]),
     "tide_group_device_status": (ctypes.c_int, [_vp, _i32p]),
     "tide_group_set_debug": (ctypes.c_int, [_vp, ctypes.c_uint32]),
@@ -241,6 +242,12 @@ def tide_group_set_ag_variant(g: int, variant: int) -> None:
     _check(lib().tide_group_set_ag_variant(g, variant), "tide_group_set_ag_variant")
 
 
+def tide_group_ag_kernel(g: int) -> int:
+    v = ctypes.c_int32()
+    _check(lib().tide_group_ag_kernel(g, ctypes.byref(v)), "tide_group_ag_kernel")
+    return v.value
+
+
 def tide_group_set_ce_lanes(g: int, lanes: int) -> None:
     _check(lib().tide_group_set_ce_lanes(g, lanes), "tide_group_set_ce_lanes")
 
@@ -363,6 +370,9 @@ class Group:
 
     def set_ag_variant(self, variant: int) -> None:
         tide_group_set_ag_variant(self.handle, variant)
+
+    def ag_kernel(self) -> int:
+        return tide_group_ag_kernel(self.handle)
 
     def set_ce_lanes(self, lanes: int) -> None:
         tide_group_set_ce_lanes(self.handle, lanes)

@@ -535,6 +535,13 @@ int tide_group_set_rs_variant(tide_group_t g, int32_t variant) {
     return TIDE_OK;
 }
 
+int tide_group_ag_kernel(tide_group_t g, int32_t* variant) {
+    if (!g || !variant) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    *variant = ag_uses_bulk(g, true) ? TIDE_AG_BULK : TIDE_AG_REGISTER;
+    return TIDE_OK;
+}
+
 int tide_group_set_ce_lanes(tide_group_t g, int32_t lanes) {
     if (!g || lanes < 1 || lanes > kMaxCeLanes) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);

@@ -292,7 +292,8 @@ def run_tide(args, rank, world, local_rank):
                            "bytes": b_rs, "ctas": rs_ctas},
         "all_gather_sm": {"gbs": b_ag / (ag_avg * 1e-3) / 1e9, "ms": ag_avg, "ms_median": statistics.median(ag_ms),
                           "bytes": b_ag, "ctas": ag_ctas,
-                          "kernel": "all_gather_kernel" if args.ag_variant == "register" else "all_gather_bulk_kernel"},
+                          "kernel": "all_gather_bulk_kernel" if G.ag_kernel() == tide.TIDE_AG_BULK
+                          else "all_gather_kernel"},
     }
     # copy-engine placement and the bulk-copy placement, same buffers (outside the step's timed region)
     legs["all_gather_ce"] = time_ce(G, buf, stream, b_ag, max(3, args.steps))

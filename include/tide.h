@@ -186,6 +186,10 @@ int tide_group_set_rs_variant(tide_group_t g, int32_t variant);
  * 16-byte aligned pointers; otherwise the register path runs. */
 int tide_group_set_ag_variant(tide_group_t g, int32_t variant);
 
+/* The placement kernel tide_all_gather runs on g under the current settings when every shard and
+ * parameter pointer is 16-byte aligned: TIDE_AG_BULK or TIDE_AG_REGISTER (resolves TIDE_AG_AUTO). */
+int tide_group_ag_kernel(tide_group_t g, int32_t *variant);
+
 /*
  * Every device-side wait of the library's kernels (the bulk paths' mbarrier waits) gives up after
  * `timeout_ns` (0 = the default, 2 s): it writes a nonzero code to the group's device status word,

@@ -97,6 +97,8 @@ def test_null_group_calls(tide):
         assert getattr(L, fn)(None, arr, arr, None) == tide.TIDE_EINVAL
     v = ctypes.c_int64()
     assert L.tide_group_shard_elems(None, ctypes.byref(v)) == tide.TIDE_EINVAL
+    k = ctypes.c_int32()
+    assert L.tide_group_ag_kernel(None, ctypes.byref(k)) == tide.TIDE_EINVAL
     assert L.tide_group_destroy(None) == tide.TIDE_OK
 
 

@@ -311,6 +311,28 @@ def _shifted_groups():
     return gs
 
 
+def test_auto_placement_choice(tide):
+    """AUTO resolves to the bulk placement for long runs or a capped CTA count, else the register
+    path; explicit choices are kept."""
+    long_runs = group("llama70b").scaled(2)  # 72 runs of 2.8 M elements on average
+    G = tide.Group(long_runs.R, list(zip(long_runs.rows, long_runs.row_len)))
+    assert G.ag_kernel() == tide.TIDE_AG_BULK
+    G.set_ctas(0, 16)
+    assert G.ag_kernel() == tide.TIDE_AG_BULK
+    G.set_ctas(0, 0)
+    G.set_ag_variant(tide.TIDE_AG_REGISTER)
+    assert G.ag_kernel() == tide.TIDE_AG_REGISTER
+    G.set_ag_variant(tide.TIDE_AG_BULK)
+    assert G.ag_kernel() == tide.TIDE_AG_BULK
+    G.close()
+    q = group("qwen3moe").scaled(4)  # 3,144 runs of 12 k elements on average
+    G = tide.Group(q.R, list(zip(q.rows, q.row_len)))
+    assert G.ag_kernel() == tide.TIDE_AG_REGISTER
+    G.set_ctas(0, 16)
+    assert G.ag_kernel() == tide.TIDE_AG_BULK
+    G.close()
+
+
 @pytest.mark.parametrize("variant", [0, 1, 2], ids=["auto", "register", "bulk"])
 @pytest.mark.parametrize("g", _shifted_groups(), ids=lambda g: g.name)
 def test_all_gather_any_relative_alignment(tide, g, variant):
