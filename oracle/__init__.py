@@ -46,6 +46,8 @@ def _configure(L: ctypes.CDLL) -> ctypes.CDLL:
     L.oracle_bf16_to_f32.restype = ctypes.c_float
     for fn in ("oracle_reduce_scatter", "oracle_exact_sum", "oracle_all_gather", "oracle_shard_bf16"):
         getattr(L, fn).argtypes = [i32, i32, _i64p, _i64p, vpp, vpp]
+    for fn in ("oracle_reduce_scatter_part", "oracle_all_gather_part"):
+        getattr(L, fn).argtypes = [i32, i32, _i64p, _i64p, vpp, vpp, i32, i32, i32]
     return L
 
 
@@ -129,6 +131,48 @@ def reduce_scatter(lay: Layout, grads: Sequence[Sequence[np.ndarray]]) -> List[n
                                      lay.row_len.ctypes.data_as(_i64p), _ptrs(flat), _ptrs(shards))
     assert rc == 0
     return shards
+
+
+class Marshalled(NamedTuple):
+    """Pointer tables of one group's host arrays, built once so that many part calls (possibly
+    from several threads; ctypes releases the GIL during each call) reuse them."""
+    lay: Layout
+    src: object
+    dst: object
+    keep: tuple  # the arrays the tables point into
+
+
+def marshal_reduce_scatter(lay: Layout, grads, shards: Sequence[np.ndarray]) -> Marshalled:
+    """Pointer tables for ``reduce_scatter_part``: ``grads[r][p]`` bf16 bits, ``shards`` R fp32
+    arrays of S elements (written in place)."""
+    flat = _check_grads(lay, grads)
+    assert len(shards) == lay.R and all(s.dtype == np.float32 and s.size >= lay.S for s in shards)
+    return Marshalled(lay, _ptrs(flat), _ptrs(shards), (flat, list(shards)))
+
+
+def reduce_scatter_part(m: Marshalled, d: int, p_begin: int, p_end: int) -> None:
+    """Destination rank ``d``'s shard elements of parameters ``p_begin <= p < p_end`` only."""
+    lay = m.lay
+    rc = lib().oracle_reduce_scatter_part(lay.R, lay.P, lay.rows.ctypes.data_as(_i64p),
+                                          lay.row_len.ctypes.data_as(_i64p), m.src, m.dst, d, p_begin, p_end)
+    assert rc == 0, rc
+
+
+def marshal_all_gather(lay: Layout, shards: Sequence[np.ndarray], params: Sequence[np.ndarray]) -> Marshalled:
+    """Pointer tables for ``all_gather_part``: R bf16 shards, P bf16 parameters (written in place)."""
+    sh = [np.ascontiguousarray(s).view(np.uint16).reshape(-1) for s in shards]
+    assert len(sh) == lay.R and all(s.size >= lay.S for s in sh)
+    pa = [p.view(np.uint16).reshape(-1) for p in params]
+    assert len(pa) == lay.P and all(pa[p].size == lay.rows[p] * lay.row_len[p] for p in range(lay.P))
+    return Marshalled(lay, _ptrs(sh), _ptrs(pa), (sh, pa))
+
+
+def all_gather_part(m: Marshalled, r: int, p_begin: int, p_end: int) -> None:
+    """Source rank ``r``'s rows of parameters ``p_begin <= p < p_end`` only."""
+    lay = m.lay
+    rc = lib().oracle_all_gather_part(lay.R, lay.P, lay.rows.ctypes.data_as(_i64p),
+                                      lay.row_len.ctypes.data_as(_i64p), m.src, m.dst, r, p_begin, p_end)
+    assert rc == 0, rc
 
 
 def exact_sum(lay: Layout, grads) -> List[np.ndarray]:

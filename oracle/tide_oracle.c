@@ -111,11 +111,17 @@ static void layout_free(oracle_layout *L)
  * padded row j < m_p and column k < L_p,
  *     shard[d][o_p + j*L_p + k] = g[0][p][i] + g[1][p][i] + ... + g[R-1][p][i]   (fp32, left fold)
  * with i = (d*m_p + j)*L_p + k when d*m_p + j < rows_p, and +0.0f otherwise.
+ *
+ * oracle_reduce_scatter_part computes that definition for one destination rank d and the
+ * parameters p_begin <= p < p_end only (it writes nothing but those elements of shards[d]), so
+ * that a caller can run disjoint parts on several host threads; oracle_reduce_scatter is the
+ * whole group, every destination rank and every parameter, one part after another.
  */
-int oracle_reduce_scatter(int32_t R, int32_t P, const int64_t *rows, const int64_t *row_len,
-                          const uint16_t *const *grads, float *const *shards)
+int oracle_reduce_scatter_part(int32_t R, int32_t P, const int64_t *rows, const int64_t *row_len,
+                               const uint16_t *const *grads, float *const *shards, int32_t d,
+                               int32_t p_begin, int32_t p_end)
 {
-    if (!grads || !shards)
+    if (!grads || !shards || d < 0 || d >= R || p_begin < 0 || p_end > P || p_begin > p_end)
         return ORACLE_EINVAL;
     oracle_layout L;
     int rc = layout_make(&L, R, P, rows, row_len);
@@ -123,26 +129,37 @@ int oracle_reduce_scatter(int32_t R, int32_t P, const int64_t *rows, const int64
         layout_free(&L);
         return rc;
     }
-    for (int32_t d = 0; d < R; ++d) {
-        for (int32_t p = 0; p < P; ++p) {
-            for (int64_t j = 0; j < L.m[p]; ++j) {
-                int64_t row = (int64_t)d * L.m[p] + j;
-                for (int64_t k = 0; k < row_len[p]; ++k) {
-                    float acc;
-                    if (row < rows[p]) {
-                        int64_t i = row * row_len[p] + k;
-                        acc = oracle_bf16_to_f32(grads[0 * (int64_t)P + p][i]);
-                        for (int32_t r = 1; r < R; ++r)
-                            acc = acc + oracle_bf16_to_f32(grads[(int64_t)r * P + p][i]);
-                    } else {
-                        acc = 0.0f;
-                    }
-                    shards[d][L.o[p] + j * row_len[p] + k] = acc;
+    for (int32_t p = p_begin; p < p_end; ++p) {
+        for (int64_t j = 0; j < L.m[p]; ++j) {
+            int64_t row = (int64_t)d * L.m[p] + j;
+            for (int64_t k = 0; k < row_len[p]; ++k) {
+                float acc;
+                if (row < rows[p]) {
+                    int64_t i = row * row_len[p] + k;
+                    acc = oracle_bf16_to_f32(grads[0 * (int64_t)P + p][i]);
+                    for (int32_t r = 1; r < R; ++r)
+                        acc = acc + oracle_bf16_to_f32(grads[(int64_t)r * P + p][i]);
+                } else {
+                    acc = 0.0f;
                 }
+                shards[d][L.o[p] + j * row_len[p] + k] = acc;
             }
         }
     }
     layout_free(&L);
+    return ORACLE_OK;
+}
+
+int oracle_reduce_scatter(int32_t R, int32_t P, const int64_t *rows, const int64_t *row_len,
+                          const uint16_t *const *grads, float *const *shards)
+{
+    if (!grads || !shards || R < 1)
+        return ORACLE_EINVAL;
+    for (int32_t d = 0; d < R; ++d) {
+        int rc = oracle_reduce_scatter_part(R, P, rows, row_len, grads, shards, d, 0, P);
+        if (rc != ORACLE_OK)
+            return rc;
+    }
     return ORACLE_OK;
 }
 
@@ -182,11 +199,16 @@ int oracle_exact_sum(int32_t R, int32_t P, const int64_t *rows, const int64_t *r
  * padded row j < m_p with r*m_p + j < rows_p,
  *     param[p][(r*m_p + j)*L_p + k] = shard[r][o_p + j*L_p + k]     for k < L_p.
  * Padding rows of the shards are never read; nothing outside the rows_p rows is written.
+ *
+ * oracle_all_gather_part places the rows of one source rank r for the parameters
+ * p_begin <= p < p_end only (disjoint parts may run on several host threads);
+ * oracle_all_gather is every source rank and every parameter, one part after another.
  */
-int oracle_all_gather(int32_t R, int32_t P, const int64_t *rows, const int64_t *row_len,
-                      const uint16_t *const *shards, uint16_t *const *params)
+int oracle_all_gather_part(int32_t R, int32_t P, const int64_t *rows, const int64_t *row_len,
+                           const uint16_t *const *shards, uint16_t *const *params, int32_t r,
+                           int32_t p_begin, int32_t p_end)
 {
-    if (!shards || !params)
+    if (!shards || !params || r < 0 || r >= R || p_begin < 0 || p_end > P || p_begin > p_end)
         return ORACLE_EINVAL;
     oracle_layout L;
     int rc = layout_make(&L, R, P, rows, row_len);
@@ -194,16 +216,28 @@ int oracle_all_gather(int32_t R, int32_t P, const int64_t *rows, const int64_t *
         layout_free(&L);
         return rc;
     }
-    for (int32_t r = 0; r < R; ++r)
-        for (int32_t p = 0; p < P; ++p)
-            for (int64_t j = 0; j < L.m[p]; ++j) {
-                int64_t row = (int64_t)r * L.m[p] + j;
-                if (row >= rows[p])
-                    continue;
-                for (int64_t k = 0; k < row_len[p]; ++k)
-                    params[p][row * row_len[p] + k] = shards[r][L.o[p] + j * row_len[p] + k];
-            }
+    for (int32_t p = p_begin; p < p_end; ++p)
+        for (int64_t j = 0; j < L.m[p]; ++j) {
+            int64_t row = (int64_t)r * L.m[p] + j;
+            if (row >= rows[p])
+                continue;
+            for (int64_t k = 0; k < row_len[p]; ++k)
+                params[p][row * row_len[p] + k] = shards[r][L.o[p] + j * row_len[p] + k];
+        }
     layout_free(&L);
+    return ORACLE_OK;
+}
+
+int oracle_all_gather(int32_t R, int32_t P, const int64_t *rows, const int64_t *row_len,
+                      const uint16_t *const *shards, uint16_t *const *params)
+{
+    if (!shards || !params || R < 1)
+        return ORACLE_EINVAL;
+    for (int32_t r = 0; r < R; ++r) {
+        int rc = oracle_all_gather_part(R, P, rows, row_len, shards, params, r, 0, P);
+        if (rc != ORACLE_OK)
+            return rc;
+    }
     return ORACLE_OK;
 }
 

@@ -56,6 +56,14 @@ def random_groups(seed: int, n: int = 6):
     return out
 
 
+def wide_bf16(seed: int, n: int, spread: int = 18) -> np.ndarray:
+    """Random finite bf16 patterns with exponents spread over 2^-spread .. 2^spread: sums of a few
+    of them need far more than fp32's 24 significant bits, but fewer than fp64's 53."""
+    rs = np.random.default_rng(seed)
+    x = (rs.standard_normal(n) * np.exp2(rs.integers(-spread, spread + 1, n))).astype(np.float32)
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
 def random_bf16(seed: int, n: int, scale: float = 1.0) -> np.ndarray:
     """Random finite bf16 bit patterns with varied exponents (fold order matters for them)."""
     rs = np.random.default_rng(seed)
@@ -305,6 +313,73 @@ def pin_rs_points(seed: int = 8):
         assert np.array_equal(_f32_bits(pts), _f32_bits(np.concatenate(full)))
 
 
+def pin_exact_sum_vs_fsum(seed: int = 10):
+    """The fp64 reference sum equals math.fsum (Shewchuk's exactly rounded sum) of the widened
+    inputs at every output position, with +0 in padding.  The inputs' exponents span 2^-18 .. 2^18,
+    so an exact sum needs up to ~45 significant bits: fp64 keeps them all, an fp32 accumulator or a
+    dropped term does not."""
+    for gi, (R, rows, row_len) in enumerate(random_groups(seed) + [(9, [4, 11], [7, 3])]):
+        lay = oracle.plan(R, rows, row_len)
+        grads = [[wide_bf16(seed * 1000 + gi * 100 + r * 10 + p, rows[p] * row_len[p])
+                  for p in range(len(rows))] for r in range(R)]
+        widened = [[oracle.bf16_to_f32(grads[r][p]).astype(np.float64) for p in range(len(rows))] for r in range(R)]
+        exact = oracle.exact_sum(lay, grads)
+        for d in range(R):
+            for p in range(len(rows)):
+                m, L = int(lay.m[p]), row_len[p]
+                for j in range(m):
+                    row = d * m + j
+                    for k in range(L):
+                        got = exact[d][int(lay.o[p]) + j * L + k]
+                        if row < rows[p]:
+                            want = math.fsum(float(widened[r][p][row * L + k]) for r in range(R))
+                            assert got == want, (R, rows, row_len, d, p, j, k, got, want)
+                        else:
+                            assert got == 0.0 and not math.copysign(1.0, got) < 0
+
+
+def pin_parts_partition_the_group(seed: int = 11):
+    """The per-(rank, parameter-range) parts write exactly their own elements (everything else keeps
+    its sentinel), and all parts together give the whole-group result bit for bit, for the
+    reduce-scatter and the all-gather alike."""
+    for gi, (R, rows, row_len) in enumerate(random_groups(seed)):
+        lay = oracle.plan(R, rows, row_len)
+        P = len(rows)
+        grads = [[random_bf16(seed * 1000 + gi * 100 + r * 10 + p, rows[p] * row_len[p])
+                  for p in range(P)] for r in range(R)]
+        full = oracle.reduce_scatter(lay, grads)
+        out = [np.full(lay.S, np.nan, np.float32) for _ in range(R)]
+        m = oracle.marshal_reduce_scatter(lay, grads, out)
+        for d in range(R):
+            for p in range(P):
+                before = [o.copy() for o in out]
+                oracle.reduce_scatter_part(m, d, p, p + 1)
+                lo, hi = int(lay.o[p]), int(lay.o[p] + lay.s[p])
+                for e in range(R):
+                    changed = _f32_bits(out[e]) != _f32_bits(before[e])
+                    if e != d:
+                        assert not changed.any()
+                    else:
+                        assert not changed[:lo].any() and not changed[hi:].any()
+                        assert np.array_equal(_f32_bits(out[e][lo:hi]), _f32_bits(full[e][lo:hi]))
+        for d in range(R):
+            assert np.array_equal(_f32_bits(out[d]), _f32_bits(full[d]))
+        shards = [random_bf16(seed * 100 + gi * 10 + r, lay.S, 0.02) for r in range(R)]
+        want = oracle.all_gather(lay, shards, [np.full(rows[p] * row_len[p], SENTINEL_BF16, np.uint16)
+                                               for p in range(P)])
+        got = [np.full(rows[p] * row_len[p], SENTINEL_BF16, np.uint16) for p in range(P)]
+        ma = oracle.marshal_all_gather(lay, shards, got)
+        for r in range(R):
+            oracle.all_gather_part(ma, r, 0, P)
+            for p in range(P):
+                v = lay.valid_rows(r, p) * row_len[p]
+                lo = r * int(lay.m[p]) * row_len[p]
+                assert np.array_equal(got[p][lo:lo + v], want[p][lo:lo + v])
+                assert np.all(got[p][lo + v:] == SENTINEL_BF16)  # later ranks' rows not yet written
+        for p in range(P):
+            assert np.array_equal(got[p], want[p])
+
+
 ALL_PINS = [
     pin_plan_golden,
     pin_hand_worked,
@@ -318,6 +393,8 @@ ALL_PINS = [
     pin_negative_zero,
     pin_ag_roundtrip,
     pin_rs_points,
+    pin_exact_sum_vs_fsum,
+    pin_parts_partition_the_group,
 ]
 
 

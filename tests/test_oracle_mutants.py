@@ -20,8 +20,8 @@ ROOT = os.path.dirname(HERE)
 
 MUTANTS = {
     "padded_rows_floor_plus_one": ("m[p] = (rows[p] + R - 1) / R;", "m[p] = rows[p] / R + 1;"),
-    "dropped_rank_term": ("for (int32_t r = 1; r < R; ++r)\n                            acc = acc +",
-                          "for (int32_t r = 2; r < R; ++r)\n                            acc = acc +"),
+    "dropped_rank_term": ("for (int32_t r = 1; r < R; ++r)\n                        acc = acc +",
+                          "for (int32_t r = 2; r < R; ++r)\n                        acc = acc +"),
     "wrong_sign": ("acc = acc + oracle_bf16_to_f32", "acc = acc - oracle_bf16_to_f32"),
     "transposed_input_index": ("int64_t i = row * row_len[p] + k;", "int64_t i = k * rows[p] + row;"),
     "transposed_output_index": ("shards[d][L.o[p] + j * row_len[p] + k] = acc;",
@@ -33,10 +33,14 @@ MUTANTS = {
     "widening_shift": ("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
     "ag_reads_global_row": ("params[p][row * row_len[p] + k] = shards[r][L.o[p] + j * row_len[p] + k];",
                             "params[p][row * row_len[p] + k] = shards[r][L.o[p] + row * row_len[p] + k];"),
-    "ag_rank_row_base": ("int64_t row = (int64_t)r * L.m[p] + j;\n                if (row >= rows[p])\n                    continue;\n                for (int64_t k = 0; k < row_len[p]; ++k)\n                    params",
-                         "int64_t row = (int64_t)r * L.s[p] + j;\n                if (row >= rows[p])\n                    continue;\n                for (int64_t k = 0; k < row_len[p]; ++k)\n                    params"),
-    "fold_from_plus_zero": ("acc = oracle_bf16_to_f32(grads[0 * (int64_t)P + p][i]);\n                        for (int32_t r = 1;",
-                            "acc = 0.0f;\n                        for (int32_t r = 0;"),
+    "ag_rank_row_base": ("int64_t row = (int64_t)r * L.m[p] + j;\n            if (row >= rows[p])\n                continue;\n            for (int64_t k = 0; k < row_len[p]; ++k)\n                params",
+                         "int64_t row = (int64_t)r * L.s[p] + j;\n            if (row >= rows[p])\n                continue;\n            for (int64_t k = 0; k < row_len[p]; ++k)\n                params"),
+    "fold_from_plus_zero": ("acc = oracle_bf16_to_f32(grads[0 * (int64_t)P + p][i]);\n                    for (int32_t r = 1;",
+                            "acc = 0.0f;\n                    for (int32_t r = 0;"),
+    "part_skips_last_param": ("for (int32_t p = p_begin; p < p_end; ++p) {", "for (int32_t p = p_begin; p + 1 < p_end; ++p) {"),
+    "exact_sum_fp32_accumulator": ("double acc = 0.0;", "float acc = 0.0f;"),
+    "exact_sum_dropped_rank_term": ("for (int32_t r = 0; r < R; ++r)\n                            acc +=",
+                                    "for (int32_t r = 1; r < R; ++r)\n                            acc +="),
 }
 
 _RUNNER = r"""
