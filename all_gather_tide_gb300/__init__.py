@@ -29,6 +29,8 @@ TIDE_ERANGE = -6
 TIDE_FLAG_VEC_STRICT = 0x1
 TIDE_FLAG_CE_STRICT = 0x2
 TIDE_FLAG_CE_2D = 0x4
+TIDE_FLAG_OVERLAP = 0x8
+TIDE_FLAG_CE_1D = 0x10
 TIDE_RS_AUTO = 0
 TIDE_RS_REGISTER = 1
 TIDE_RS_BULK = 2
@@ -61,6 +63,7 @@ SIGNATURES = {
     "tide_group_set_rs_variant": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "tide_group_set_ag_variant": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "tide_group_set_ce_lanes": (ctypes.c_int, [_vp, ctypes.c_int32]),
+    "tide_group_set_ce_bands": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "tide_group_ag_kernel": (ctypes.c_int, [_vp, _i32p]),
     "tide_group_set_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_uint64]),
     "tide_group_device_status": (ctypes.c_int, [_vp, _i32p]),
@@ -69,6 +72,8 @@ SIGNATURES = {
     "tide_probe_hold": (ctypes.c_int, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64,
                                        _vp, _vp]),
     "tide_probe_bulk_read": (ctypes.c_int, [_vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]),
+    "tide_probe_ingest": (ctypes.c_int, [_vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]),
     "tide_stage_into_slots": (ctypes.c_int, [_vp, _vpp, _vpp, ctypes.c_int64, _vpp, _vp]),
     "tide_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "tide_last_cuda_error": (ctypes.c_int, []),
@@ -252,6 +257,10 @@ def tide_group_set_ce_lanes(g: int, lanes: int) -> None:
     _check(lib().tide_group_set_ce_lanes(g, lanes), "tide_group_set_ce_lanes")
 
 
+def tide_group_set_ce_bands(g: int, bands: int) -> None:
+    _check(lib().tide_group_set_ce_bands(g, bands), "tide_group_set_ce_bands")
+
+
 def tide_group_set_wait_timeout(g: int, timeout_ns: int) -> None:
     _check(lib().tide_group_set_wait_timeout(g, timeout_ns), "tide_group_set_wait_timeout")
 
@@ -304,6 +313,14 @@ def tide_probe_bulk_read(buf, nbytes: int, ctas: int, copy_bytes: int, stages: i
     """Bulk-copy read bandwidth probe; ``out`` is a device uint32/int32 tensor of 2 entries."""
     _check(lib().tide_probe_bulk_read(_ptr(buf), nbytes, ctas, copy_bytes, stages, _ptr(out), _stream(stream)),
            "tide_probe_bulk_read")
+
+
+def tide_probe_ingest(buf, bulk_bytes: int, ldg_bytes: int, ctas: int, copy_bytes: int, stages: int,
+                      consumer_warps: int, ldg_warps: int, out, stream=None) -> None:
+    """Per-SM ingest probe (bulk copies read out of shared memory and/or 32-byte register loads);
+    ``out`` is a device uint32/int32 tensor of 2 entries."""
+    _check(lib().tide_probe_ingest(_ptr(buf), bulk_bytes, ldg_bytes, ctas, copy_bytes, stages, consumer_warps,
+                                   ldg_warps, _ptr(out), _stream(stream)), "tide_probe_ingest")
 
 
 # ---- convenience object -----------------------------------------------------------------------
@@ -376,6 +393,9 @@ class Group:
 
     def set_ce_lanes(self, lanes: int) -> None:
         tide_group_set_ce_lanes(self.handle, lanes)
+
+    def set_ce_bands(self, bands: int) -> None:
+        tide_group_set_ce_bands(self.handle, bands)
 
     def set_wait_timeout(self, timeout_ns: int) -> None:
         tide_group_set_wait_timeout(self.handle, timeout_ns)

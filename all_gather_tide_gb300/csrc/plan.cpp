@@ -127,4 +127,46 @@ void make_work_lists(Plan* pl) {
     pl->ag_bulk_chunks = chunks;
 }
 
+int plan_rs_pieces(int32_t R, int32_t P, const int64_t* rows, const int64_t* row_len, RsSeg* out, size_t cap,
+                   int64_t* nchunks) {
+    if (!rows || !row_len || !out || !nchunks || R < 1 || R > TIDE_MAX_RANKS || P < 1) return TIDE_EINVAL;
+    if (size_t(R) * size_t(P) > cap) return TIDE_ERANGE;
+    // pass 1: check every parameter and count the chunks of one destination rank's pieces
+    int64_t per_rank = 0, off = 0, total = 0;
+    for (int32_t p = 0; p < P; ++p) {
+        if (rows[p] < 1 || row_len[p] < 1) return TIDE_EINVAL;
+        const int64_t m = rows[p] / R + (rows[p] % R != 0);
+        int64_t s, n, Rm;
+        if (!mul_ok(m, row_len[p], &s) || !mul_ok(rows[p], row_len[p], &n) || !mul_ok(m, R, &Rm) ||
+            !mul_ok(Rm, row_len[p], &Rm) || !add_ok(off, s, &off))
+            return TIDE_ERANGE;
+        per_rank += (s + kRsChunk - 1) / kRsChunk;
+    }
+    if (!mul_ok(off, R, &total) || !mul_ok(total, 4, &total) || !mul_ok(per_rank, R, &total)) return TIDE_ERANGE;
+    // pass 2: the pieces in make_work_lists' order (destination-major, parameter order within a
+    // shard), with their chunk ranges in the flat chunk list
+    off = 0;
+    int64_t before = 0;  // chunks of parameters 0..p-1 in one rank's list
+    for (int32_t p = 0; p < P; ++p) {
+        const int64_t m = rows[p] / R + (rows[p] % R != 0);
+        const int64_t s = m * row_len[p];
+        for (int32_t d = 0; d < R; ++d) {
+            RsSeg sg{};
+            sg.dst_off = off;
+            sg.src_off = int64_t(d) * s;
+            sg.valid = valid_rows(rows[p], m, d) * row_len[p];
+            sg.total = s;
+            sg.chunk_begin = int64_t(d) * per_rank + before;
+            sg.d = d;
+            sg.p = p;
+            sg.vec = sg.src_off % 8 == 0;
+            out[size_t(d) * size_t(P) + size_t(p)] = sg;
+        }
+        off += s;
+        before += (s + kRsChunk - 1) / kRsChunk;
+    }
+    *nchunks = per_rank * R;
+    return TIDE_OK;
+}
+
 }  // namespace tide

@@ -5,7 +5,9 @@
 // CTAs shaped like the GEMM's clusters, each occupying a whole SM, write down the SM number and
 // the arrival and departure times, so CTAs displaced past the first wave, and the SMs a collective keeps, can be counted.
 // A third probe measures how fast one SM's bulk-copy engine reads as a function of the copy size,
-// the fact the bulk-copy reduce-scatter is built around.
+// the fact the bulk-copy reduce-scatter is built around; a fourth how many bytes per second one SM
+// can bring in at all (bulk copies read out of shared memory, wide register loads, or both at once),
+// which bounds any reduce-scatter that may hold only a few SMs.
 //
 // Every loop here is bounded by %globaltimer or by the buffer size; nothing waits on another launch.
 #include <algorithm>
@@ -128,6 +130,142 @@ __global__ void bulk_read_kernel(const unsigned char* __restrict__ buf, int64_t 
     }
 }
 
+// 32-byte streaming register load (eight 32-bit words).
+struct W8 {
+    uint32_t w[8];
+};
+__device__ __forceinline__ void ld32(const unsigned char* p, W8& r) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r.w[0]), "=r"(r.w[1]), "=r"(r.w[2]), "=r"(r.w[3]), "=r"(r.w[4]), "=r"(r.w[5]), "=r"(r.w[6]),
+                   "=r"(r.w[7])
+                 : "l"(p));
+}
+
+constexpr int kIngestLoads = 8;  // register loads in flight per thread
+
+// Warp 0 lane 0 streams [buf, buf + bulk_bytes) through `stages` slots of `copy_bytes` bulk copies
+// (the CTAs' copies a grid stride apart); warps 1..consumers read every 16-byte word of a landed
+// slot (`read_all`) or only its first word, then release it; the next `ldg_warps` warps stream
+// [ldg, ldg + ldg_bytes) with 32-byte loads, kIngestLoads in flight per thread.  Every wait is
+// bounded (1 s): on expiry out[1] gets a flag and the CTA winds down after its copies have landed.
+__global__ void __launch_bounds__(512, 1)
+ingest_kernel(const unsigned char* __restrict__ buf, int64_t bulk_bytes, const unsigned char* __restrict__ ldg,
+              int64_t ldg_bytes, int copy_bytes, int stages, int consumers, int read_all, int ldg_warps,
+              uint32_t* out) {
+    extern __shared__ __align__(128) unsigned char sm[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm);
+    uint64_t* empty = full + 16;
+    unsigned char* data = sm + 256;
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&full[s])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&empty[s])), "r"(consumers));
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    volatile int* abort = &abort_flag;
+    const uint64_t limit = 1000000000ull;
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const uint64_t t0 = now_ns();
+        uint32_t n = 0, ok = 0;
+        while (true) {
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(ok)
+                : "r"(smem_u32(bar)), "r"(parity)
+                : "memory");
+            if (ok) return true;
+            if ((++n & 255) == 0) {
+                if (*abort) return false;
+                if (now_ns() - t0 > limit) {
+                    *abort = 1;
+                    atomicOr(&out[1], 1u);
+                    return false;
+                }
+            }
+        }
+    };
+    const int64_t nchunk = bulk_bytes / copy_bytes;
+    uint32_t x = 0;
+    if (warp == 0) {
+        if (lane == 0 && nchunk > 0) {
+            int64_t k = 0;
+            for (int64_t c = blockIdx.x; c < nchunk; c += gridDim.x, ++k) {
+                const int s = int(k % stages);
+                if (!wait(&empty[s], uint32_t(((k / stages) & 1) ^ 1))) break;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&full[s])),
+                             "r"(copy_bytes)
+                             : "memory");
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        smem_u32(data + int64_t(s) * copy_bytes)),
+                    "l"(buf + c * copy_bytes), "r"(copy_bytes), "r"(smem_u32(&full[s]))
+                    : "memory");
+            }
+            // every issued copy lands before the CTA exits (bounded)
+            const uint64_t t0 = now_ns();
+            for (int64_t j = k > stages ? k - stages : 0; j < k; ++j) {
+                uint32_t ok = 0;
+                while (!ok) {
+                    asm volatile(
+                        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                        "selp.u32 %0, 1, 0, p;\n\t}"
+                        : "=r"(ok)
+                        : "r"(smem_u32(&full[j % stages])), "r"(uint32_t((j / stages) & 1))
+                        : "memory");
+                    if (!ok && now_ns() - t0 > limit) {
+                        atomicOr(&out[1], 2u);
+                        break;
+                    }
+                }
+            }
+        }
+    } else if (warp <= consumers) {
+        const int ctid = (warp - 1) * 32 + lane;
+        const int words = copy_bytes / 16;
+        int64_t k = 0;
+        for (int64_t c = blockIdx.x; c < nchunk; c += gridDim.x, ++k) {
+            const int s = int(k % stages);
+            if (!wait(&full[s], uint32_t((k / stages) & 1))) break;
+            const uint4* row = reinterpret_cast<const uint4*>(data + int64_t(s) * copy_bytes);
+            if (read_all) {
+                for (int i = ctid; i < words; i += consumers * 32) {
+                    const uint4 w = row[i];
+                    x ^= w.x ^ w.y ^ w.z ^ w.w;
+                }
+            } else if (ctid == 0) {
+                x ^= row[0].x;
+            }
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[s])) : "memory");
+        }
+    } else if (warp <= consumers + ldg_warps) {
+        const int64_t nthreads = int64_t(gridDim.x) * ldg_warps * 32;
+        const int64_t tid = int64_t(blockIdx.x) * ldg_warps * 32 + (warp - consumers - 1) * 32 + lane;
+        const int64_t nvec = ldg_bytes / 32;
+        for (int64_t v = tid; v < nvec; v += nthreads * kIngestLoads) {
+            W8 r[kIngestLoads];
+#pragma unroll
+            for (int u = 0; u < kIngestLoads; ++u) {
+                const int64_t q = v + int64_t(u) * nthreads;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) r[u].w[i] = 0;
+                if (q < nvec) ld32(ldg + q * 32, r[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < kIngestLoads; ++u)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x ^= r[u].w[i];
+        }
+    }
+    if (x) atomicXor(&out[0], x);
+}
+
 }  // namespace
 }  // namespace tide
 
@@ -167,6 +305,26 @@ int tide_probe_bulk_read(const void* buf, int64_t bytes, int32_t ctas, int32_t c
     if (e != cudaSuccess) return tide::record_cuda_error(e);
     tide::bulk_read_kernel<<<ctas, 64, smem, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const unsigned char*>(buf), bytes, copy_bytes, stages, out);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TIDE_OK : tide::record_cuda_error(e);
+}
+
+int tide_probe_ingest(const void* buf, int64_t bulk_bytes, int64_t ldg_bytes, int32_t ctas, int32_t copy_bytes,
+                      int32_t stages, int32_t consumer_warps, int32_t ldg_warps, uint32_t* out, void* stream) {
+    const int consumers = consumer_warps > 0 ? consumer_warps : 1;
+    if (!buf || !out || bulk_bytes < 0 || ldg_bytes < 0 || ctas < 1 || copy_bytes < 16 || copy_bytes % 16 ||
+        stages < 1 || stages > 16 || int64_t(copy_bytes) * stages > 220 * 1024 || consumer_warps < 0 ||
+        ldg_warps < 0 || 1 + consumers + ldg_warps > 16 || (reinterpret_cast<uintptr_t>(buf) & 255u) ||
+        ldg_bytes % 32)
+        return TIDE_EINVAL;
+    const int smem = 256 + copy_bytes * stages;
+    cudaError_t e = cudaFuncSetAttribute(tide::ingest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return tide::record_cuda_error(e);
+    const auto* base = static_cast<const unsigned char*>(buf);
+    const int64_t ldg_off = (bulk_bytes + 255) / 256 * 256;  // the register loads' region follows, 256-byte aligned
+    tide::ingest_kernel<<<ctas, 32 * (1 + consumers + ldg_warps), smem, static_cast<cudaStream_t>(stream)>>>(
+        base, bulk_bytes, base + ldg_off, ldg_bytes, copy_bytes, stages, consumers, consumer_warps > 0 ? 1 : 0,
+        ldg_warps, out);
     e = cudaGetLastError();
     return e == cudaSuccess ? TIDE_OK : tide::record_cuda_error(e);
 }

@@ -6,11 +6,12 @@
 // kernel is limited by the bytes one SM keeps in flight; this variant keeps a deep pipeline of
 // bulk copies in flight per SM instead.
 //
-// The bulk-copy engine of an SM keeps only a few copies in flight, so its bandwidth grows with the
-// size of each copy (measured on GB300: about 17 GB/s per SM with 4 KB copies, about 185 GB/s per
-// SM with 48 KB copies).  The kernel therefore streams one rank's row of a chunk per copy: a chunk
-// is kBulkChunk elements of one (destination, parameter) piece, and its R rows pass through
-// up to kBulkMaxStages shared-memory stages of kBulkChunk bf16 elements, rank 0 first.  The fp32 sums of
+// The bulk-copy engine of an SM keeps only about four copies in flight, so its bandwidth grows with
+// the size of each copy (measured on GB300 at 16 CTAs: about 17 GB/s per SM with 4 KB copies, 68
+// with 16 KB, 136 with 32 KB, 190 with 46-72 KB).  The kernel therefore streams one rank's row of a
+// chunk per copy: a chunk is kBulkChunk elements of one (destination, parameter) piece, and its R
+// rows pass through up to kBulkMaxStages shared-memory stages of kBulkChunk bf16 elements (45 KB),
+// rank 0 first.  The fp32 sums of
 // the chunk stay in the consumers' registers across the R stages (ascending rank order, starting
 // from rank 0's value, exact bf16 -> fp32 widening, __fadd_rn), and are stored once, straight to
 // the destination shard (st.global.cs), after the last rank.
@@ -284,20 +285,25 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, const int32_t* __rest
             }
             if (__shfl_sync(0xffffffffu, stop, 0)) break;
         }
-        // On abort, let the copies already issued land before the CTA's shared memory goes away.
+        // Let every copy already issued land before the CTA's shared memory goes away, whether the
+        // producer ran out of chunks or stopped early: a consumer wait that expires after the
+        // producer issued its last copy must not leave copies writing into freed shared memory.
         // Only the last `stages` stage uses can still be in flight, and each is the newest phase
         // of its stage, so waiting for that phase's parity is exact.
-        if (lane == 0 && *abort && !inject) {
+        if (lane == 0 && !inject) {
             const uint64_t drain = globaltimer() + 100000000ull;  // at most 100 ms
             for (int64_t j = max(int64_t(0), it - stages); j < it; ++j) {
                 uint64_t* bar = &full[j % stages];
                 const uint32_t par = uint32_t((j / stages) & 1);
+                bool late = false;
                 while (!mbar_try_wait(bar, par)) {
                     if (globaltimer() > drain) {
                         atomicCAS(status, 0, 4);
+                        late = true;
                         break;
                     }
                 }
+                if (late) break;
             }
         }
         return;

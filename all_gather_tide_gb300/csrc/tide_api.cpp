@@ -13,6 +13,8 @@ namespace {
 
 constexpr int kSlots = 4;  // pointer-table ring depth
 constexpr int kMaxCeLanes = 8;  // helper streams for copy-engine work
+constexpr uint32_t kAllFlags =
+    TIDE_FLAG_VEC_STRICT | TIDE_FLAG_CE_STRICT | TIDE_FLAG_CE_2D | TIDE_FLAG_OVERLAP | TIDE_FLAG_CE_1D;
 
 thread_local int g_last_cuda_error = 0;
 
@@ -71,6 +73,7 @@ struct tide_group {
     // copy-engine work is spread over `ce_lanes` streams forked from and joined back to the
     // caller's stream, so several copy engines run at once
     int ce_lanes = kMaxCeLanes;  // measured on GB300: 1-D copies over 8 streams reach ~0.94 x HBM peak
+    int ce_bands = 1;  // 2-D copies per parameter (bands of ranks)
     cudaStream_t lane_stream[kMaxCeLanes] = {};
     cudaEvent_t lane_done[kMaxCeLanes] = {};
     cudaEvent_t fork = nullptr;
@@ -204,6 +207,25 @@ struct CeLanes {
 
 int default_ctas(const tide_group* g, int per_sm) { return std::max(1, g->sm_count * per_sm); }
 
+// CTA budget of a group created with TIDE_FLAG_OVERLAP: about a ninth of the SMs (16 on a 152-SM
+// GB300).  Measured on GB300 beside a single-wave cuBLAS bf16 GEMM (4096 x 4096 x 8192, 4-CTA
+// clusters, one CTA per SM): up to 16 resident SM-filling CTAs cost it nothing, 20 cost one tile
+// round (~16 %).
+int overlap_ctas(const tide_group* g) { return std::max(1, g->sm_count / 9); }
+
+bool overlap_mode(const tide_group* g) { return (g->flags & TIDE_FLAG_OVERLAP) != 0; }
+
+// The placement's CTA count when the caller has not set one.
+int ag_default_ctas(const tide_group* g, bool bulk) {
+    if (overlap_mode(g)) return overlap_ctas(g);
+    return default_ctas(g, bulk ? tide::kAgBulkCtasPerSm : tide::kAgCtasPerSm);
+}
+
+int rs_default_ctas(const tide_group* g, bool bulk) {
+    if (overlap_mode(g)) return overlap_ctas(g);
+    return bulk ? g->sm_count : default_ctas(g, tide::kRsCtasPerSm);
+}
+
 // The bulk-copy placement needs 16-byte aligned pointers and moves only runs whose offsets are
 // 16-byte compatible (the rest go through three warps per CTA).  TIDE_AG_AUTO takes it when at
 // least 90 % of the elements can ride bulk copies and either the CTA count is capped below the SM
@@ -216,13 +238,31 @@ bool ag_uses_bulk(const tide_group* g, bool aligned) {
     if (!aligned || !g->d_ag_bulk || g->ag_variant == TIDE_AG_REGISTER) return false;
     if (g->ag_variant == TIDE_AG_BULK) return true;
     if (g->plan.ag_vec_elems * 10 < g->plan.U * 9) return false;
-    if (g->ag_ctas > 0 && g->ag_ctas < g->sm_count) return true;
+    const int capped = g->ag_ctas > 0 ? g->ag_ctas : (overlap_mode(g) ? overlap_ctas(g) : 0);
+    if (capped > 0 && capped < g->sm_count) return true;
     return g->plan.ag.empty() || g->plan.U >= int64_t(g->plan.ag.size()) * (int64_t(1) << 20);
 }
 
 // Bulk-copy kernel unless the register path is asked for; it needs 16-byte aligned gradient
 // pointers (the register path's element-wise fallback covers the rest).  Measured on GB300 it is the faster of
 // the two at every CTA count, most of all when the count is capped below the SM count.
+// Copy-engine form when the caller fixes none (neither TIDE_FLAG_CE_1D nor TIDE_FLAG_CE_2D): the
+// host spends about 2 us submitting each copy, so the 1-D form (one copy per (rank, parameter)
+// run, up to 6.4 TB/s over 8 lanes) is host-bound when runs are short, while the 2-D form (one
+// strided copy per parameter) holds ~3.5 TB/s on every workload measured on GB300.  The 1-D form
+// wins while runs average >= 8 MiB (Llama-3.1-70B layer 48 MB: 6.5 against 3.7 TB/s; 8B layer
+// 12 MB: 5.0 against 3.6; Wan R = 8, 11 MB: 3.8 against 3.5), the 2-D form below (Wan R = 16,
+// 5.6 MB: 3.5 against 2.5; Qwen3 MoE layer, 0.8 MB: 2.6 against 0.37).  Under TIDE_FLAG_OVERLAP
+// the 1-D form over one lane is kept whatever the run length: strided copies slowed a concurrent
+// GEMM far more per byte (+149 % against +4 % on the 70B layer).
+constexpr int64_t kCe1dMinAvgRunBytes = int64_t(8) << 20;
+
+bool ce_auto_prefers_2d(const tide_group* g) {
+    if (g->flags & TIDE_FLAG_OVERLAP) return false;
+    const int64_t runs = int64_t(g->plan.ag.size());
+    return runs > 0 && 2 * g->plan.U < runs * kCe1dMinAvgRunBytes;
+}
+
 bool use_bulk(const tide_group* g, bool aligned) {
     if (!aligned || g->plan.rs_bulk.empty() || !g->d_rs_bulk || !g->d_rs_bulk_piece) return false;
     return g->rs_variant != TIDE_RS_REGISTER;
@@ -267,6 +307,9 @@ int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* ro
                       uint32_t flags) {
     if (!out) return TIDE_EINVAL;
     *out = nullptr;
+    if (flags & ~kAllFlags) return TIDE_EINVAL;
+    if ((flags & TIDE_FLAG_CE_1D) && (flags & (TIDE_FLAG_CE_2D | TIDE_FLAG_CE_STRICT))) return TIDE_EINVAL;
+    *out = nullptr;
     tide::Plan pl;
     int rc = tide::make_layout(R, P, rows, row_len, &pl);
     if (rc != TIDE_OK) return rc;
@@ -281,6 +324,7 @@ int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* ro
     if (!g) return TIDE_ENOMEM;
     g->plan = std::move(pl);
     g->flags = flags;
+    if (flags & TIDE_FLAG_OVERLAP) g->ce_lanes = 1;
     cudaError_t e = cudaGetDevice(&g->device);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g->sm_count, cudaDevAttrMultiProcessorCount, g->device);
     if (e != cudaSuccess) {
@@ -383,10 +427,8 @@ int tide_group_set_ctas(tide_group_t g, int32_t rs_ctas, int32_t ag_ctas) {
 int tide_group_get_ctas(tide_group_t g, int32_t* rs_ctas, int32_t* ag_ctas) {
     if (!g || !rs_ctas || !ag_ctas) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);
-    *rs_ctas = g->rs_ctas ? g->rs_ctas
-                          : (g->rs_variant == TIDE_RS_REGISTER ? default_ctas(g, tide::kRsCtasPerSm) : g->sm_count);
-    *ag_ctas = g->ag_ctas ? g->ag_ctas
-                          : default_ctas(g, ag_uses_bulk(g, true) ? tide::kAgBulkCtasPerSm : tide::kAgCtasPerSm);
+    *rs_ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, g->rs_variant != TIDE_RS_REGISTER);
+    *ag_ctas = g->ag_ctas ? g->ag_ctas : ag_default_ctas(g, ag_uses_bulk(g, true));
     return TIDE_OK;
 }
 
@@ -418,12 +460,12 @@ int tide_reduce_scatter(tide_group_t g, const void* const* grads, void* const* s
     auto* sp = reinterpret_cast<float* const*>(dev + size_t(R) * P);
     cudaError_t e;
     if (use_bulk(g, aligned)) {
-        const int ctas = g->rs_ctas ? g->rs_ctas : g->sm_count;
+        const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, true);
         e = tide::launch_reduce_scatter_bulk(g->d_rs_bulk, g->d_rs_bulk_piece, g->plan.rs_bulk_chunks, gp, sp,
                                              R, P, 1, ctas, g->d_status, g->timeout_ns,
                                              (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
     } else {
-        const int ctas = g->rs_ctas ? g->rs_ctas : default_ctas(g, tide::kRsCtasPerSm);
+        const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, false);
         e = tide::launch_reduce_scatter(g->d_rs, int(g->plan.rs.size()), g->d_rs_piece, g->plan.rs_chunks, gp, sp,
                                         R, P, aligned ? 1 : 0, ctas, st);
     }
@@ -458,11 +500,11 @@ int tide_all_gather(tide_group_t g, const void* const* shards, void* const* para
     auto* pp = reinterpret_cast<uint16_t* const*>(dev + R);
     cudaError_t e;
     if (ag_uses_bulk(g, aligned)) {
-        const int ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgBulkCtasPerSm);
+        const int ctas = g->ag_ctas ? g->ag_ctas : ag_default_ctas(g, true);
         e = tide::launch_all_gather_bulk(g->d_ag_bulk, int(g->plan.ag_bulk.size()), g->plan.ag_bulk_chunks, sp, pp,
                                          ctas, g->d_status, g->timeout_ns, st);
     } else {
-        const int ctas = g->ag_ctas ? g->ag_ctas : default_ctas(g, tide::kAgCtasPerSm);
+        const int ctas = g->ag_ctas ? g->ag_ctas : ag_default_ctas(g, false);
         e = tide::launch_all_gather(g->d_ag, int(g->plan.ag.size()), g->d_ag_run, g->plan.ag_chunks, sp, pp,
                                     aligned ? 1 : 0, ctas, st);
     }
@@ -484,8 +526,11 @@ int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* p
     const int64_t pitch = R > 1 ? static_cast<const char*>(shards[1]) - base : pl.S * 2;
     bool uniform = pitch >= pl.S * 2;
     for (int r = 1; r < R && uniform; ++r) uniform = static_cast<const char*>(shards[r]) == base + int64_t(r) * pitch;
-    if (!(g->flags & TIDE_FLAG_CE_2D)) uniform = false;  // default: one 1-D copy per (rank, parameter) run
-    else if (!uniform && (g->flags & TIDE_FLAG_CE_STRICT)) return TIDE_ELAYOUT;
+    if (g->flags & TIDE_FLAG_CE_2D) {
+        if (!uniform && (g->flags & TIDE_FLAG_CE_STRICT)) return TIDE_ELAYOUT;
+    } else if ((g->flags & TIDE_FLAG_CE_1D) || !ce_auto_prefers_2d(g)) {
+        uniform = false;  // one 1-D copy per (rank, parameter) run
+    }
     int rc = check_device(g);
     if (rc != TIDE_OK) return rc;
     CeLanes lanes{g, static_cast<cudaStream_t>(stream)};
@@ -495,13 +540,17 @@ int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* p
         char* dst = static_cast<char*>(params[p]);
         const int64_t piece_bytes = pl.s[p] * 2;
         if (uniform) {
-            // ranks 0 .. f-1 hold full pieces of m_p rows: one 2-D copy, source rows `pitch`
-            // apart, destination rows contiguous
+            // ranks 0 .. f-1 hold full pieces of m_p rows: one 2-D copy per band of ranks (one band
+            // by default: the whole parameter in one strided copy), source rows `pitch` apart,
+            // destination rows contiguous
             const int64_t f = pl.rows[p] / pl.m[p];
-            if (f > 0) {
-                TIDE_CUDA(cudaMemcpy2DAsync(dst, size_t(piece_bytes), base + pl.o[p] * 2, size_t(pitch),
-                                            size_t(piece_bytes), size_t(f), cudaMemcpyDeviceToDevice,
-                                            lanes.pick(f * piece_bytes)));
+            const int64_t nb = std::min<int64_t>(g->ce_bands, f);
+            for (int64_t b = 0; b < nb; ++b) {
+                const int64_t r0 = f * b / nb, r1 = f * (b + 1) / nb;
+                TIDE_CUDA(cudaMemcpy2DAsync(dst + r0 * piece_bytes, size_t(piece_bytes),
+                                            base + r0 * pitch + pl.o[p] * 2, size_t(pitch), size_t(piece_bytes),
+                                            size_t(r1 - r0), cudaMemcpyDeviceToDevice,
+                                            lanes.pick((r1 - r0) * piece_bytes)));
                 ++copies;
             }
             const int64_t rest = pl.rows[p] - f * pl.m[p];
@@ -549,6 +598,13 @@ int tide_group_set_ce_lanes(tide_group_t g, int32_t lanes) {
     return TIDE_OK;
 }
 
+int tide_group_set_ce_bands(tide_group_t g, int32_t bands) {
+    if (!g || bands < 1 || bands > TIDE_MAX_RANKS) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    g->ce_bands = bands;
+    return TIDE_OK;
+}
+
 int tide_group_set_ag_variant(tide_group_t g, int32_t variant) {
     if (!g || variant < TIDE_AG_AUTO || variant > TIDE_AG_BULK) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);
@@ -559,7 +615,7 @@ int tide_group_set_ag_variant(tide_group_t g, int32_t variant) {
 int tide_group_set_wait_timeout(tide_group_t g, uint64_t timeout_ns) {
     if (!g) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);
-    g->timeout_ns = timeout_ns ? timeout_ns : tide::kDefaultTimeoutNs;
+    g->timeout_ns = timeout_ns ? std::max(timeout_ns, tide::kMinTimeoutNs) : tide::kDefaultTimeoutNs;
     return TIDE_OK;
 }
 

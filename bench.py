@@ -42,8 +42,7 @@ from workloads import Group, group, rng  # noqa: E402
 
 METRIC = "RS/AG effective HBM GB/s and % of GB300 peak; concurrent GEMM slowdown %"
 FALLBACK_HBM_GBS = 6800.0
-# Bounded sample of the workload for the host-side oracle: these parameters of the group.
-CPU_SAMPLE_PARAMS = ("k", "v", "o", "input_norm", "post_norm")
+DATA = "synthetic (seeded counter-based N(0,1e-3) gradients, N(0,0.02) shards; layer shapes only)"
 
 
 def workload(args) -> Group:
@@ -59,6 +58,15 @@ def layout(g: Group):
 
     m, s, o, S, U = tide.tide_plan_layout(g.R, g.rows, g.row_len)
     return S, U
+
+
+def workload_config(g: Group, S: int, U: int, replicas: int) -> dict:
+    """The workload a step processes, the same dict for the GPU arm and the reference arm."""
+    step_bytes = rs_bytes(g, S, U) + ag_bytes(U)
+    return {"workload": g.name, "R": g.R, "P": g.P, "U": U, "S": S,
+            "step": "reduce-scatter + all-gather placement of the whole group", "step_bytes": step_bytes,
+            "l2": f"inputs larger than L2 ({step_bytes / 1e9:.1f} GB of traffic per step), no flush",
+            "replicas": replicas}
 
 
 def rs_bytes(g: Group, S: int, U: int) -> int:
@@ -325,12 +333,9 @@ def run_tide(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "f32",
         "io_dtypes": {"grads": "bf16", "rs_shards": "f32", "ag_shards": "bf16", "params": "bf16"},
-        "data": "synthetic (seeded counter-based N(0,1e-3) gradients, N(0,0.02) shards; layer shapes only)",
-        "config": {"workload": g.name, "R": g.R, "P": g.P, "U": U, "S": S,
-                   "step": "reduce_scatter + all_gather (SM kernel)",
-                   "step_bytes": step_bytes, "rs_ctas": rs_ctas, "ag_ctas": ag_ctas,
-                   "l2": f"inputs larger than L2 ({step_bytes / 1e9:.1f} GB of traffic per step), no flush",
-                   "replicas": world},
+        "data": DATA,
+        "config": workload_config(g, S, U, world),
+        "launch": {"rs_ctas": rs_ctas, "ag_ctas": ag_ctas, "step": "tide_reduce_scatter + tide_all_gather (SM kernel)"},
         "legs": legs,
         "gpu_launches": 2 * args.steps,
     }
@@ -358,9 +363,7 @@ def run_tide(args, rank, world, local_rank):
         out["e2e"] = end_to_end(G, g, buf, S, U, dev, args, world)
         out["e2e"]["host_affinity"] = numa
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(g, dev, reps=args.cpu_reps)
-        out["cpu_baseline"]["cpu_model"] = cpu_model()
-        out["cpu_baseline_all_cores"] = cpu_baseline_all_cores(g, dev)
+        out["cpu_baseline"] = cpu_baseline(g, dev, passes=args.cpu_passes)
     G.close()
     return out
 
@@ -388,37 +391,20 @@ def time_ce(G, buf, stream, b_ag, iters):
 def stock_comparator(G, g, buf, S, U, stream, legs):
     """The layout-converting path the paper compares against (Table 1's full-group pack, Table 7's
     copy-out column, Table 8, whose FSDP2 numbers count the _chunk_cat pack), emulated on one GPU with plain
-    PyTorch ops: every contributor packs its per-parameter bf16 gradients into a full-group fp32
-    buffer ([R, S] per contributor, zero padding; torch._chunk_cat as FSDP2 does), the packed
-    buffers are summed per destination (the reduce-scatter), and the all-gather output, a flat
-    rank-major buffer, is copied out into padded per-parameter storage (split_with_sizes_copy).
+    PyTorch ops (``all_gather_tide_gb300.stock``): every contributor packs its per-parameter bf16
+    gradients into a full-group fp32 buffer, the packed buffers are summed per destination (the
+    reduce-scatter), and the all-gather output is copied out into padded per-parameter storage.
     Timed with CUDA events; reported against the same algorithmic bytes as the direct path."""
-    R, P = g.R, g.P
-    m = [(r + R - 1) // R for r in g.rows]  # padded rows (the comparator's own arithmetic)
-    sizes = [m[p] * g.row_len[p] for p in range(P)]
-    packed = torch.empty(R, R, S, dtype=torch.float32, device=buf.shards.device)
-    out_shards = torch.empty(R, S, dtype=torch.float32, device=buf.shards.device)
-    padded = [torch.empty(R, sizes[p], dtype=torch.bfloat16, device=buf.shards.device) for p in range(P)]
-    views = [[buf.grads[r][p].view(g.rows[p], g.row_len[p]) for p in range(P)] for r in range(R)]
-    have_chunk_cat = hasattr(torch, "_chunk_cat")
+    from all_gather_tide_gb300.stock import StockPath
 
-    def pack(r):
-        if have_chunk_cat:
-            torch._chunk_cat(views[r], 0, R, out=packed[r])
-        else:  # same layout by hand: chunk d of every parameter, zero-padded, concatenated
-            packed[r].zero_()
-            for p in range(P):
-                for d, piece in enumerate(torch.chunk(views[r][p], R, dim=0)):
-                    o = sum(sizes[:p])
-                    packed[r, d, o:o + piece.numel()].copy_(piece.reshape(-1))
+    sp = StockPath(g.R, g.rows, g.row_len, buf.shards.device)
+    out_shards = torch.empty(g.R, S, dtype=torch.float32, device=buf.shards.device)
 
     def rs():
-        for r in range(R):
-            pack(r)
-        torch.sum(packed, dim=0, out=out_shards)
+        sp.reduce_scatter(buf.grads, out_shards)
 
     def ag():
-        torch.split_with_sizes_copy(buf.ag_in.view(R, S), sizes, dim=1, out=padded)
+        sp.copy_out(buf.ag_in)
 
     def timed(fn, reps=3):
         with torch.cuda.stream(stream):
@@ -438,25 +424,28 @@ def stock_comparator(G, g, buf, S, U, stream, legs):
     sms = torch.cuda.get_device_properties(buf.shards.device).multi_processor_count
     rs_ctas0, ag_ctas0 = G.get_ctas()
     G.set_ctas(16, ag_ctas0)
-    ms16 = timed(lambda: G.reduce_scatter(buf.grads, buf.shard_list))
+    ms16 = timed(lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream))
     G.set_ctas(rs_ctas0, ag_ctas0)
     direct_ms, direct_ctas = legs["reduce_scatter"]["ms"], legs["reduce_scatter"]["ctas"]
     sm_time = {"stock_sm_ms": rs_ms * sms, "direct_sm_ms": direct_ms * min(direct_ctas, sms),
                "direct_16ctas_ms": ms16, "direct_16ctas_sm_ms": ms16 * 16,
                "ratio_full_width": rs_ms * sms / (direct_ms * min(direct_ctas, sms)),
                "ratio_16ctas": rs_ms * sms / (ms16 * 16)}
+    # the direct path's shards (last written by the full-width call above) against the stock sums
+    G.reduce_scatter(buf.grads, buf.shard_list, stream)
+    torch.cuda.synchronize()
+    err = (out_shards - buf.shards).abs().max().item()
     res = {
         "reduce_scatter": {"ms": rs_ms, "gbs_of_direct_bytes": b_rs / (rs_ms * 1e-3) / 1e9,
                            "direct_ms": legs["reduce_scatter"]["ms"], "speedup_direct": rs_ms / legs["reduce_scatter"]["ms"],
-                           "extra_buffer_bytes": packed.numel() * 4, "pack": "torch._chunk_cat" if have_chunk_cat else "chunk+copy",
-                           "sm_time": sm_time},
+                           "extra_buffer_bytes": sp.extra_buffer_bytes,
+                           "pack": "torch._chunk_cat" if sp.have_chunk_cat else "chunk+copy",
+                           "sm_time": sm_time, "max_abs_diff_vs_direct": err},
         "all_gather_copy_out": {"ms": ag_ms, "gbs_of_direct_bytes": b_ag / (ag_ms * 1e-3) / 1e9,
                                 "direct_ms": legs["all_gather_sm"]["ms"], "speedup_direct": ag_ms / legs["all_gather_sm"]["ms"],
                                 "op": "torch.split_with_sizes_copy into padded [R, m_p*L_p] storage"},
     }
-    err = (out_shards - buf.shards).abs().max().item()
-    res["reduce_scatter"]["max_abs_diff_vs_direct"] = err
-    del packed, out_shards, padded
+    del sp, out_shards
     torch.cuda.empty_cache()
     return res
 
@@ -590,12 +579,55 @@ def interference(G, buf, stream, dev, args):
     if args.sweep:
         out["cta_sweep"] = cta_sweep(G, buf, stream, args, concurrent)
     rs_default, ag_default = G.get_ctas()
+    b_rs, b_ag = rs_bytes_of(G), 4 * G.U
+    peak, peak_kind = hbm_peak()
+
+    def alone_ms(launch, reps=2):
+        with torch.cuda.stream(stream):
+            launch()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                launch()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
     out["reduce_scatter"] = dict(ctas=rs_default, **concurrent(lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream), "rs"))
+    # the reduce-scatter at capped CTA counts: bandwidth alone and beside the GEMM, and the GEMM's
+    # slowdown; the operating point is the largest count that keeps the slowdown <= 10 %
+    rs_rows = []
     for n_ctas in args.interference_ctas:
         G.set_ctas(n_ctas, 0)
-        out[f"reduce_scatter_ctas{n_ctas}"] = dict(ctas=n_ctas, **concurrent(
-            lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream), "rs"))
+        launch = lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream)
+        ms = alone_ms(launch)
+        conc = concurrent(launch, "rs")
+        row = dict(ctas=n_ctas, gbs_alone=b_rs / (ms * 1e-3) / 1e9,
+                   gbs_beside_gemm=b_rs / (conc["collective_ms"] * 1e-3) / 1e9, **conc)
+        out[f"reduce_scatter_ctas{n_ctas}"] = row
+        rs_rows.append(row)
     G.set_ctas(args.rs_ctas, args.ag_ctas)
+    ok = [r for r in rs_rows if r["slowdown_pct"] is not None and r["slowdown_pct"] <= 10.0]
+    if ok:
+        best = max(ok, key=lambda r: r["gbs_beside_gemm"])
+        out["operating_point"] = {
+            "ctas": best["ctas"], "gemm_slowdown_pct": best["slowdown_pct"], "victim_rate": best["victim_rate"],
+            "rs_gbs_beside_gemm": best["gbs_beside_gemm"], "frac_beside_gemm": best["gbs_beside_gemm"] / peak,
+            "rs_gbs_alone": best["gbs_alone"], "frac_alone": best["gbs_alone"] / peak, "peak": peak,
+            "peak_kind": peak_kind, "target_frac": 0.75, "target_slowdown_pct": 10.0,
+            "joint_target_met": bool(best["gbs_beside_gemm"] / peak >= 0.75),
+            "rule": "largest reduce-scatter bandwidth beside the GEMM among the CTA counts with <= 10 % slowdown"}
+    # what 16 SMs could move at best: the measured per-SM ingest ceiling x 16, scaled from bytes
+    # read to the reduce-scatter's algorithmic bytes (reads R*U*2 of the R*U*2 + R*S*4)
+    ing = sm_ingest(dev, stream, ctas=16)
+    read_bytes = 2 * G.R * G.U
+    bound = 16 * ing["ceiling_gbs_per_sm"] * b_rs / read_bytes
+    out["sm_ingest_16_ctas"] = ing
+    if "operating_point" in out:
+        out["operating_point"]["bound_16_sms_gbs"] = bound
+        out["operating_point"]["bound_16_sms_frac"] = bound / peak
+        out["operating_point"]["bound_rule"] = ("16 x the measured per-SM ingest ceiling x (algorithmic bytes / "
+                                                "bytes read): no kernel on 16 SMs can exceed it")
     # the placement is short; run it several times back to back so GEMMs fit inside
     out["all_gather_sm"] = dict(ctas=ag_default, **concurrent(
         lambda: [G.all_gather(buf.ag_list, buf.params, stream) for _ in range(8)], "ag"))
@@ -606,7 +638,76 @@ def interference(G, buf, stream, dev, args):
     out["all_gather_ce_lanes1"] = dict(ctas=0, ce_lanes=1, **concurrent(
         lambda: [G.all_gather_ce(buf.ag_list, buf.params, stream) for _ in range(8)], "ce"))
     G.set_ce_lanes(args.ce_lanes or 8)
+    # plain calls on a group created with TIDE_FLAG_OVERLAP (interference-first defaults)
+    import all_gather_tide_gb300 as tide
+
+    Gov = tide.Group(G.R, list(zip(G.rows, G.row_len)), tide.TIDE_FLAG_OVERLAP)
+    ov_rs, ov_ag = Gov.get_ctas()
+    legs = (("reduce_scatter", lambda: Gov.reduce_scatter(buf.grads, buf.shard_list, stream), b_rs, ov_rs),
+            ("all_gather_sm", lambda: [Gov.all_gather(buf.ag_list, buf.params, stream) for _ in range(8)], 8 * b_ag,
+             ov_ag),
+            ("all_gather_ce", lambda: [Gov.all_gather_ce(buf.ag_list, buf.params, stream) for _ in range(8)],
+             8 * b_ag, 0))
+    ov = {}
+    for name, launch, nbytes, ctas in legs:
+        ms = alone_ms(launch)
+        conc = concurrent(launch, name)
+        ov[name] = dict(ctas=ctas, gbs_alone=nbytes / (ms * 1e-3) / 1e9, frac_alone=nbytes / (ms * 1e-3) / 1e9 / peak,
+                        gbs_beside_gemm=nbytes / (conc["collective_ms"] * 1e-3) / 1e9, **conc)
+    ov["all_gather_sm"]["kernel"] = "all_gather_bulk_kernel" if Gov.ag_kernel() == tide.TIDE_AG_BULK else "all_gather_kernel"
+    ov["all_gather_ce"]["copies"], ov["all_gather_ce"]["uniform_pitch"] = Gov.last_ce_copies()
+    ov["flag"] = "TIDE_FLAG_OVERLAP"
+    out["overlap_mode"] = ov
+    Gov.close()
     return out
+
+
+def sm_ingest(dev, stream, full=False, ctas=16):
+    """Bytes per second one SM can bring in (tide_probe_ingest, `ctas` CTAs, one per SM, over a
+    4 GiB buffer): bulk copies alone, bulk copies read out of shared memory, 32-byte register loads,
+    and both at once.  The largest is the ceiling of any kernel that reads its inputs through that
+    many SMs."""
+    import all_gather_tide_gb300 as tide
+
+    nb = 4 << 30
+    buf = torch.empty(nb // 4, dtype=torch.int32, device=dev)
+    buf.fill_(0x3C00_3C00)
+    out = torch.zeros(2, dtype=torch.int32, device=dev)
+    cases = [("bulk copies only", 73728, 3, 0, 0, 1.0), ("bulk copies read out", 46080, 5, 15, 0, 1.0),
+             ("bulk copies read out", 73728, 3, 15, 0, 1.0), ("register loads only", 32768, 1, 1, 14, 0.0),
+             ("both", 65536, 3, 8, 7, 0.6), ("both", 65536, 3, 8, 7, 0.7)]
+    if full:
+        cases += [("bulk copies only", 46080, 5, 0, 0, 1.0), ("bulk copies read out", 57344, 4, 14, 0, 1.0),
+                  ("bulk copies read out", 65536, 3, 15, 0, 1.0), ("register loads only", 32768, 1, 1, 8, 0.0),
+                  ("both", 65536, 3, 11, 4, 0.8)]
+
+    def launch(copy, stages, cons, ldgw, f):
+        bulk = int(nb * f) // copy * copy
+        ldg = (nb - (bulk + 255) // 256 * 256) // 32 * 32 if ldgw else 0
+        tide.tide_probe_ingest(buf, bulk, ldg, ctas, copy, stages, cons, ldgw, out, stream)
+        return bulk + ldg
+
+    with torch.cuda.stream(stream):
+        for _ in range(30):  # bring the clocks up
+            launch(73728, 3, 15, 0, 1.0)
+    torch.cuda.synchronize()
+    rows = []
+    for name, copy, stages, cons, ldgw, f in cases:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            launch(copy, stages, cons, ldgw, f)
+            ev[0].record(stream)
+            n = sum(launch(copy, stages, cons, ldgw, f) for _ in range(3))
+            ev[1].record(stream)
+        torch.cuda.synchronize()
+        gbs = n / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
+        rows.append({"mode": name, "copy_bytes": copy, "stages": stages, "consumer_warps": cons,
+                     "ldg_warps": ldgw, "bulk_fraction": f, "gbs": gbs, "gbs_per_sm": gbs / ctas})
+    assert int(out[1].item()) == 0, "a probe wait expired"
+    del buf
+    torch.cuda.empty_cache()
+    best = max(rows, key=lambda r: r["gbs_per_sm"])
+    return {"ctas": ctas, "rows": rows, "ceiling_gbs_per_sm": best["gbs_per_sm"], "ceiling_mode": best["mode"]}
 
 
 def cta_sweep(G, buf, stream, args, concurrent):
@@ -808,6 +909,7 @@ def probes(G, buf, stream, dev, args):
     G.set_ce_lanes(args.ce_lanes or 8)
     G2.close()
     out["table4_table5"] = rows
+    out["sm_ingest"] = {n: sm_ingest(dev, stream, full=True, ctas=n) for n in (16, sms)}
     del a2, b2, c2, x, y, z
     torch.cuda.empty_cache()
     return out
@@ -921,44 +1023,15 @@ def end_to_end(G, g, buf, S, U, dev, args, world):
 # ---- the host oracle ---------------------------------------------------------------------------
 
 
-def cpu_sample(g: Group, names=CPU_SAMPLE_PARAMS):
-    params = tuple(p for p in g.params if p[0] in names) or g.params[:1]
-    return Group(g.name + "-sample", g.R, params, g.grad_kind, g.grad_sigma, g.shard_sigma, g.grad_seed,
-                 g.grad_seed_per_rank, g.shard_seed_base)
-
-
-def cpu_inputs(sub: Group, S: int, dev):
+def cpu_inputs(g: Group, S: int, dev):
+    """The workload's inputs as host arrays (bf16 bits): every rank's gradients and all-gather
+    shards, drawn by the same seeded generator as the device buffers (on the GPU when there is one,
+    then copied to the host)."""
     where = dev if (dev is not None and torch.cuda.is_available()) else "cpu"
-    grads = [[rng.grad_bits(sub, r, p, device=where).cpu().numpy().view(np.uint16) for p in range(sub.P)]
-             for r in range(sub.R)]
-    shards = [rng.shard_bits(sub, r, S, device=where).cpu().numpy().view(np.uint16) for r in range(sub.R)]
+    grads = [[rng.grad_bits(g, r, p, device=where).cpu().numpy().view(np.uint16) for p in range(g.P)]
+             for r in range(g.R)]
+    shards = [rng.shard_bits(g, r, S, device=where).cpu().numpy().view(np.uint16) for r in range(g.R)]
     return grads, shards
-
-
-def oracle_step(oracle, lay, grads, shards, params):
-    oracle.reduce_scatter(lay, grads)
-    oracle.all_gather(lay, shards, params)
-
-
-def cpu_baseline(g: Group, dev, reps: int = 4):
-    import oracle
-
-    sub = cpu_sample(g)
-    lay = oracle.plan(sub.R, sub.rows, sub.row_len)
-    grads, shards = cpu_inputs(sub, lay.S, dev)
-    params = [np.empty(sub.numel(p), np.uint16) for p in range(sub.P)]
-    nbytes = rs_bytes(sub, lay.S, lay.U) + ag_bytes(lay.U)
-    oracle_step(oracle, lay, grads, shards, params)  # warm
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        oracle_step(oracle, lay, grads, shards, params)
-    dt = time.perf_counter() - t0
-    return {"value": nbytes * reps / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "seconds": dt,
-            "sample": f"{g.name} restricted to {', '.join(p[0] for p in sub.params)} "
-                      f"({lay.U} of the group's elements per rank-set; reduce-scatter + all-gather, "
-                      f"{reps} passes), single-threaded C oracle",
-            "host_cpus": os.cpu_count()}
 
 
 def cpu_model() -> str:
@@ -973,79 +1046,102 @@ def cpu_model() -> str:
     return platform.processor() or platform.machine()
 
 
-def _oracle_replica(sub: Group, grads, shards, reps: int, warmup: int, barrier, results) -> None:
-    """One host process of an all-cores oracle run: the unchanged single-threaded oracle on its own
-    copy of the sample's inputs, started with the others through a barrier."""
-    import oracle
+class HostOracle:
+    """The unchanged single-threaded C oracle run over the WHOLE workload on the host's cores: one
+    pass = the reduce-scatter and the all-gather placement of the full group, split into
+    independent parts (one per (destination rank, parameter) and (source rank, parameter)), which
+    a pool of host threads takes largest first (ctypes releases the GIL during each call, so the
+    threads run in parallel).  Every part keeps the oracle's own loops and order."""
 
-    lay = oracle.plan(sub.R, sub.rows, sub.row_len)
-    params = [np.empty(sub.numel(p), np.uint16) for p in range(sub.P)]
-    for _ in range(max(1, warmup)):
-        oracle_step(oracle, lay, grads, shards, params)
-    barrier.wait(timeout=600)
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        oracle_step(oracle, lay, grads, shards, params)
-    results.put(time.perf_counter() - t0)
+    def __init__(self, g: Group, dev=None):
+        import oracle
+
+        oracle.build()
+        self.g = g
+        self.lay = oracle.plan(g.R, g.rows, g.row_len)
+        self.grads, self.shards = cpu_inputs(g, self.lay.S, dev)
+        self.out = [np.empty(self.lay.S, np.float32) for _ in range(g.R)]
+        self.params = [np.empty(g.numel(p), np.uint16) for p in range(g.P)]
+        self.m_rs = oracle.marshal_reduce_scatter(self.lay, self.grads, self.out)
+        self.m_ag = oracle.marshal_all_gather(self.lay, self.shards, self.params)
+        rs = [("rs", d, p, int(self.lay.s[p]) * (2 * g.R + 4)) for d in range(g.R) for p in range(g.P)]
+        ag = [("ag", r, p, self.lay.valid_rows(r, p) * int(self.lay.row_len[p]) * 4)
+              for r in range(g.R) for p in range(g.P)]
+        self.tasks = sorted(rs, key=lambda t: -t[3]) + sorted((t for t in ag if t[3]), key=lambda t: -t[3])
+        self.bytes_per_pass = rs_bytes(g, self.lay.S, self.lay.U) + ag_bytes(self.lay.U)
+
+    def _run(self, task):
+        import oracle
+
+        kind, a, p, _ = task
+        if kind == "rs":
+            oracle.reduce_scatter_part(self.m_rs, a, p, p + 1)
+        else:
+            oracle.all_gather_part(self.m_ag, a, p, p + 1)
+
+    def time_passes(self, passes: int, warmup: int, threads: int) -> float:
+        """Seconds for `passes` whole-group passes on `threads` host threads, after `warmup`.  The
+        reduce-scatter parts all finish before the all-gather parts start, as in one step."""
+        from concurrent.futures import ThreadPoolExecutor
+
+        rs = [t for t in self.tasks if t[0] == "rs"]
+        ag = [t for t in self.tasks if t[0] == "ag"]
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            def one_pass():
+                list(ex.map(self._run, rs))
+                list(ex.map(self._run, ag))
+
+            for _ in range(warmup):
+                one_pass()
+            t0 = time.perf_counter()
+            for _ in range(passes):
+                one_pass()
+            return time.perf_counter() - t0
 
 
-def oracle_replicas(g: Group, dev=None, reps: int = 8, warmup: int = 1) -> dict:
-    """The oracle on every host core this process may use: one replica process per core (spawned,
-    never forked from a CUDA process), each running the single-threaded oracle over the k and v
-    matrices of the layer on its own copy of the inputs (drawn once here and sent to each replica);
-    value = the bytes all replicas moved / the slowest replica's time."""
-    import multiprocessing as mp
-
-    import oracle
-
-    oracle.build()
-    n = len(os.sched_getaffinity(0))
-    sub = cpu_sample(g, ("k", "v"))
-    lay = oracle.plan(sub.R, sub.rows, sub.row_len)
-    grads, shards = cpu_inputs(sub, lay.S, dev)
-    nbytes = rs_bytes(sub, lay.S, lay.U) + ag_bytes(lay.U)
-    ctx = mp.get_context("spawn")
-    barrier, results = ctx.Barrier(n), ctx.Queue()
-    procs = [ctx.Process(target=_oracle_replica, args=(sub, grads, shards, reps, warmup, barrier, results),
-                         daemon=True) for _ in range(n)]
-    for p in procs:
-        p.start()
-    try:
-        times = [results.get(timeout=900) for _ in range(n)]
-    finally:
-        for p in procs:
-            p.join(timeout=60)
-            if p.is_alive():
-                p.kill()
-    return {"value": n * nbytes * reps / max(times) / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
-            "seconds": max(times),
-            "sample": f"{n} processes, each the single-threaded C oracle on its own copy of {g.name} restricted "
-                      f"to {', '.join(p[0] for p in sub.params)} ({lay.U} elements per rank-set; reduce-scatter "
-                      f"+ all-gather, {reps} passes)",
-            "cpu_model": cpu_model()}
+def host_threads() -> int:
+    return len(os.sched_getaffinity(0))
 
 
-def cpu_baseline_all_cores(g: Group, dev=None, reps: int = 8) -> dict:
-    return oracle_replicas(g, dev, reps)
+def cpu_baseline(g: Group, dev, passes: int = 3) -> dict:
+    """The oracle as it stands, on every host core this process may use, over the whole workload
+    (the reduce-scatter and the placement of the full group, the same bytes as one GPU step); and
+    one pass on a single thread for scale."""
+    ho = HostOracle(g, dev)
+    n = host_threads()
+    dt = ho.time_passes(passes, 1, n)
+    dt1 = ho.time_passes(1, 0, 1)
+    res = {"value": ho.bytes_per_pass * passes / dt / 1e9, "unit": "GB/s", "cores": n, "kind": "oracle",
+           "seconds": dt, "passes": passes,
+           "sample": f"the whole {g.name} group (R = {g.R}, P = {g.P}): reduce-scatter + all-gather placement, "
+                     f"{ho.bytes_per_pass / 1e9:.2f} GB of algorithmic traffic per pass, {passes} passes after 1 "
+                     f"warm-up, {n} host threads over (rank, parameter) parts of the single-threaded C oracle",
+           "one_thread_gbs": ho.bytes_per_pass / dt1 / 1e9,
+           "host_cpus": os.cpu_count(), "cpu_model": cpu_model()}
+    del ho
+    return res
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle, as it stands (single-threaded C), timed on all the host
-    cores this process may use — one replica per core, each on its own copy of a bounded sample of
-    the same workload — under the same metric.  A step = one reduce-scatter + all-gather of the
-    sample on every replica."""
+    """The reference arm: the CPU oracle, as it stands (single-threaded C loops), over the same
+    workload as the GPU arm, on all the host cores this process may use (threads over (rank,
+    parameter) parts).  A step = one reduce-scatter + all-gather placement of the whole group."""
     g = workload(args)
     dev = torch.device("cuda", 0) if torch.cuda.is_available() else None
-    res = oracle_replicas(g, dev, reps=args.steps, warmup=args.warmup)
-    value = res["value"]
+    ho = HostOracle(g, dev)
+    n = host_threads()
+    dt = ho.time_passes(args.steps, args.warmup, n)
+    value = ho.bytes_per_pass * args.steps / dt / 1e9
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": res["seconds"] * 1e3 / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (same generator and workload shapes)",
-        "config": {"workload": g.name, "R": g.R, "P": g.P, "sample_params": ["k", "v"],
-                   "step": "reduce_scatter + all_gather on the host oracle, one replica per core"},
-        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": res["cores"], "kind": "oracle",
-                         "sample": res["sample"], "cpu_model": res["cpu_model"]},
+        "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": DATA,
+        "config": workload_config(g, ho.lay.S, ho.lay.U, 1),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": n, "kind": "oracle",
+                         "sample": f"the whole {g.name} group per step (no sampling), {n} host threads over "
+                                   f"(rank, parameter) parts of the single-threaded C oracle",
+                         "cpu_model": cpu_model(), "host_cpus": os.cpu_count()},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -1065,9 +1161,9 @@ def main():
     ap.add_argument("--ag-variant", choices=["auto", "register", "bulk"], default="auto")
     ap.add_argument("--ce-lanes", type=int, default=0, help="copy-engine streams (0 = library default)")
     ap.add_argument("--ce-lanes-sweep", type=int, nargs="*", default=[])
-    ap.add_argument("--interference-ctas", type=int, nargs="*", default=[16, 32])
+    ap.add_argument("--interference-ctas", type=int, nargs="*", default=[8, 12, 16, 20, 24, 32])
     ap.add_argument("--e2e-steps", type=int, default=5)
-    ap.add_argument("--cpu-reps", type=int, default=4)
+    ap.add_argument("--cpu-passes", type=int, default=3, help="whole-group oracle passes of the CPU baseline")
     ap.add_argument("--sweep", action="store_true", help="CTA-count sweep of bandwidth vs GEMM slowdown")
     ap.add_argument("--sweep-rs", type=int, nargs="*", default=[8, 16, 20, 24, 32, 48, 64, 96, 152, 304])
     ap.add_argument("--sweep-ag", type=int, nargs="*", default=[8, 16, 24, 32, 64, 152, 608])

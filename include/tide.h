@@ -63,9 +63,24 @@ extern "C" {
 /* With TIDE_FLAG_CE_2D: return TIDE_ELAYOUT from tide_all_gather_ce instead of falling back to
  * 1-D copies when shards[r] != shards[0] + r*pitch for one pitch >= S*2 bytes. */
 #define TIDE_FLAG_CE_STRICT 0x2u
-/* tide_all_gather_ce issues one 2-D copy per parameter (the paper's form, about P copies) instead
- * of the default one 1-D copy per (rank, parameter) run of valid rows (R*P copies). */
+/* tide_all_gather_ce always issues one 2-D copy per parameter (the paper's form, about P copies;
+ * see tide_group_set_ce_bands) when the shards sit at a uniform pitch. */
 #define TIDE_FLAG_CE_2D 0x4u
+/*
+ * Interference-first defaults, for collectives that run beside compute (Fig. 3, Fig. 4, Table 4):
+ * both SM kernels launch about a ninth of the SMs as CTAs (16 on a 152-SM GB300) instead of filling
+ * the GPU, and tide_all_gather_ce uses one copy-engine lane and the 1-D form.  Measured on GB300
+ * beside a single-wave cuBLAS bf16 GEMM (4096 x 4096 x 8192): the GEMM slows by a few percent
+ * instead of +1400 % (reduce-scatter), +290 % (SM placement) and +60 % (copy engines, 8 lanes) at
+ * the throughput-first defaults, while the collectives move a quarter to two thirds as many bytes
+ * per second.  Without this flag the defaults are throughput-first: every SM, eight lanes.
+ * tide_group_set_ctas / tide_group_set_ce_lanes still override either default.
+ */
+#define TIDE_FLAG_OVERLAP 0x8u
+/* tide_all_gather_ce always issues one 1-D copy per (rank, parameter) run of valid rows (R*P
+ * copies at most).  Not combinable with TIDE_FLAG_CE_2D or TIDE_FLAG_CE_STRICT.  With neither
+ * TIDE_FLAG_CE_1D nor TIDE_FLAG_CE_2D the form is chosen per group (see tide_all_gather_ce). */
+#define TIDE_FLAG_CE_1D 0x10u
 
 typedef struct tide_group *tide_group_t;
 
@@ -84,7 +99,9 @@ int tide_plan_layout(int32_t R, int32_t P, const int64_t *rows, const int64_t *r
  * tide_group_create — plan a group (abstract; Fig. 1; Table 2) and upload its work tables to
  * the current device.  `flags` is a bitwise OR of TIDE_FLAG_*.  On success *out owns the plan;
  * on error *out is set to NULL.
- * Errors: as tide_plan_layout, plus TIDE_ERANGE (R*P > TIDE_MAX_TABLE), TIDE_ENOMEM, TIDE_ECUDA.
+ * Errors: as tide_plan_layout, plus TIDE_EINVAL (an unknown flag, or TIDE_FLAG_CE_1D with
+ * TIDE_FLAG_CE_2D or TIDE_FLAG_CE_STRICT), TIDE_ERANGE (R*P > TIDE_MAX_TABLE), TIDE_ENOMEM,
+ * TIDE_ECUDA.
  */
 int tide_group_create(tide_group_t *out, int32_t R, int32_t P, const int64_t *rows,
                       const int64_t *row_len, uint32_t flags);
@@ -103,11 +120,11 @@ int tide_group_param_layout(tide_group_t g, int32_t p, int64_t *m_p, int64_t *o_
 int tide_group_valid_rows(tide_group_t g, int32_t d, int32_t p, int64_t *v);
 
 /*
- * CTA counts of the reduce-scatter and all-gather kernels.  0 restores the default (enough
- * CTAs to fill every SM: one per SM for the bulk-copy reduce-scatter, two for its register path,
- * four per SM for either placement kernel); a positive value is used as given (at most the work's
- * chunk count),
- * so a caller can leave SMs to concurrent compute (Fig. 3, Fig. 4, Table 4).
+ * CTA counts of the reduce-scatter and all-gather kernels.  0 restores the default: throughput-
+ * first, enough CTAs to fill every SM (one per SM for the bulk-copy reduce-scatter, two for its
+ * register path, four per SM for either placement kernel), or, for a group created with
+ * TIDE_FLAG_OVERLAP, sm_count / 9 CTAs for both.  A positive value is used as given (at most the
+ * work's chunk count), so a caller can leave SMs to concurrent compute (Fig. 3, Fig. 4, Table 4).
  */
 int tide_group_set_ctas(tide_group_t g, int32_t rs_ctas, int32_t ag_ctas);
 int tide_group_get_ctas(tide_group_t g, int32_t *rs_ctas, int32_t *ag_ctas);
@@ -147,16 +164,22 @@ int tide_all_gather(tide_group_t g, const void *const *shards, void *const *para
 
 /*
  * tide_all_gather_ce — the same placement with copy engines and no SM kernel (Table 1: the
- * all-gather takes no SM; Fig. 5b).  By default one cudaMemcpyAsync per (rank, parameter) run of valid rows,
- * spread over the group's copy-engine lanes (tide_group_set_ce_lanes; default 8): measured on
- * GB300 this is the fast form for runs of several MB (Llama-3.1-70B layer: 6.4 TB/s), but the host
- * spends ~2 us submitting each copy, so groups of hundreds of short runs (Qwen3 MoE layer: 3,144
- * copies, 0.37 TB/s) do better with the 2-D form (2.6 TB/s there, ~3.5 TB/s on the other groups).
- * With TIDE_FLAG_CE_2D, and when shards[r] = shards[0] + r*pitch for
- * one pitch >= S*2 bytes, each parameter instead takes the paper's one strided copy: one
- * cudaMemcpy2DAsync over its full ranks (height f_p = floor(rows_p/m_p), width s_p*2 bytes) plus at
- * most one cudaMemcpyAsync for the rank holding its last partial piece; without a uniform pitch it
- * falls back to the 1-D copies (or returns TIDE_ELAYOUT under TIDE_FLAG_CE_STRICT).
+ * all-gather takes no SM; Fig. 5b).  Two forms:
+ *   - 1-D: one cudaMemcpyAsync per (rank, parameter) run of valid rows, spread over the group's
+ *     copy-engine lanes (tide_group_set_ce_lanes; default 8).  Measured on GB300 this is the fast
+ *     form for runs of several MB (Llama-3.1-70B layer: 6.4 TB/s), but the host spends ~2 us
+ *     submitting each copy, so groups of hundreds of short runs are host-bound (Qwen3 MoE layer:
+ *     3,144 copies, 0.37 TB/s).
+ *   - 2-D (the paper's one strided copy per parameter), when shards[r] = shards[0] + r*pitch for
+ *     one pitch >= S*2 bytes: one cudaMemcpy2DAsync over each parameter's full ranks (height
+ *     f_p = floor(rows_p/m_p), width s_p*2 bytes; or one per band of ranks, see
+ *     tide_group_set_ce_bands) plus at most one cudaMemcpyAsync for the rank holding its last
+ *     partial piece.  ~3.5 TB/s on every workload measured, 2.6 TB/s on the Qwen3 MoE layer.
+ * TIDE_FLAG_CE_1D or TIDE_FLAG_CE_2D fixes the form (TIDE_FLAG_CE_2D falls back to 1-D without a
+ * uniform pitch, or returns TIDE_ELAYOUT under TIDE_FLAG_CE_STRICT).  With neither flag the group
+ * takes the 2-D form when the pitch is uniform and its runs average less than 8 MiB, else the 1-D
+ * form; under TIDE_FLAG_OVERLAP always the 1-D form (the strided copies slow a concurrent GEMM far
+ * more per byte moved).
  */
 int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *params,
                        void *stream);
@@ -239,6 +262,13 @@ int tide_stage_into_slots(tide_group_t g, const void *const *grads, void *const 
  */
 int tide_group_set_ce_lanes(tide_group_t g, int32_t lanes);
 
+/*
+ * Splits each parameter's 2-D copy (the uniform-pitch form of tide_all_gather_ce) into up to
+ * `bands` 2-D copies over consecutive bands of ranks, spread over the copy-engine lanes like the
+ * 1-D copies (1..TIDE_MAX_RANKS, default 1: the paper's single strided copy per parameter).
+ */
+int tide_group_set_ce_bands(tide_group_t g, int32_t bands);
+
 /* Copies issued by the last tide_all_gather_ce on g, and whether the uniform-pitch form was used. */
 int tide_group_last_ce_copies(tide_group_t g, int64_t *copies, int32_t *uniform_pitch);
 
@@ -254,21 +284,24 @@ int tide_group_last_ce_copies(tide_group_t g, int64_t *copies, int32_t *uniform_
  * cannot afford cudaMalloc/cudaFree (they may synchronise the device) while communication runs
  * beside compute, can call this instead.  It takes the group description and the pointers
  * directly (same meaning and layout as tide_group_create + tide_reduce_scatter), plans the group
- * on the host at every call, copies the work tables into a fixed device array of
- * TIDE_NOALLOC_SCRATCH_BYTES that the library carries (every GPU that loads the library holds it
- * until the process exits), and launches the reduce-scatter kernel with the default CTA count.
- * It calls no cudaMalloc, cudaFree or other allocating CUDA routine.
+ * on the host at every call into a fixed host array (no heap allocation), copies the work tables
+ * into a fixed device array of TIDE_NOALLOC_SCRATCH_BYTES that the library carries (every GPU that
+ * loads the library holds it until the process exits), and launches the register-path
+ * reduce-scatter kernel with its default CTA count (two per SM).  It calls no cudaMalloc, cudaFree
+ * or other allocating CUDA routine, and no allocating host routine either.
  *   - Size limit: the tables take round_up(56*R*P, 256) + 8*(R*P + R) bytes; a group whose
- *     tables do not fit in TIDE_NOALLOC_SCRATCH_BYTES is rejected with TIDE_ERANGE before
- *     anything is enqueued.
+ *     tables do not fit in TIDE_NOALLOC_SCRATCH_BYTES (e.g. R = 8 with P > 2047) is rejected
+ *     with TIDE_ERANGE before anything is enqueued.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current; make that first call before any stream capture.
  *   - Every call shares the one array, which keeps the last call's tables; nothing in it has to
  *     start at zero, because each call rewrites everything its kernel reads.  Calls on the same
  *     stream are ordered; calls that overlap on the GPU (different streams, or several host
- *     threads on different streams) race on the array and must not be issued.
- * Errors: as tide_plan_layout and tide_reduce_scatter (no TIDE_FLAG_VEC_STRICT: unaligned pointers
- * take the element-wise path), TIDE_ERANGE as above, TIDE_ECUDA.
+ *     threads on different streams) race on the array and must not be issued.  Host threads
+ *     calling at once are serialised while the tables are written and copied.
+ * Errors: TIDE_EINVAL (as tide_plan_layout and tide_reduce_scatter; no TIDE_FLAG_VEC_STRICT:
+ * unaligned gradients take the element-wise path), TIDE_ERANGE as above or on int64 overflow,
+ * TIDE_ECUDA, TIDE_ENOMEM (the host runtime failed to lock a mutex).  No C++ exception leaves it.
  */
 int tide_reduce_scatter_noalloc(int32_t R, int32_t P, const int64_t *rows, const int64_t *row_len,
                                 const void *const *grads, void *const *shards, void *stream);
@@ -294,6 +327,24 @@ int tide_probe_hold(int32_t ctas, int32_t threads, int32_t smem_bytes, int32_t c
  */
 int tide_probe_bulk_read(const void *buf, int64_t bytes, int32_t ctas, int32_t copy_bytes, int32_t stages,
                          uint32_t *out, void *stream);
+
+/*
+ * tide_probe_ingest — how many bytes per second one SM can bring in, the bound of any reduce-scatter
+ * allowed only a few SMs (Fig. 4, Table 4: the pages' collectives hold 4 to 20 CTAs).  `ctas` CTAs
+ * (each claims copy_bytes*stages of shared memory, so one per SM) read the device buffer `buf`
+ * (256-byte aligned) in two parts at once:
+ *   - [buf, buf + bulk_bytes): bulk copies of `copy_bytes` (multiple of 16) through `stages`
+ *     shared-memory slots (copy_bytes*stages <= 220 KB, stages <= 16), each landed slot read out by
+ *     `consumer_warps` warps, every 16-byte word (0: only its first word, the copy engine alone);
+ *     whole copies only (bulk_bytes / copy_bytes of them);
+ *   - the next ldg_bytes (a multiple of 32) from buf + round_up(bulk_bytes, 256): `ldg_warps` warps
+ *     of 32-byte register loads, eight in flight per thread.
+ * 1 + max(consumer_warps, 1) + ldg_warps <= 16.  The caller's buffer must hold both parts.
+ * out (device, 2 uint32): out[0] ^= XOR checksum of what was read, out[1] |= 1 if a wait (1 s bound)
+ * expired, 2 if copies were still landing 1 s after the last issue.  TIDE_EINVAL on bad arguments.
+ */
+int tide_probe_ingest(const void *buf, int64_t bulk_bytes, int64_t ldg_bytes, int32_t ctas, int32_t copy_bytes,
+                      int32_t stages, int32_t consumer_warps, int32_t ldg_warps, uint32_t *out, void *stream);
 
 /* ---- errors ------------------------------------------------------------------------------ */
 const char *tide_strerror(int status);

@@ -79,6 +79,10 @@ def test_create_rejects_bad_arguments_before_cuda(tide):
     assert _create_status(tide, 2, [], []) == tide.TIDE_EINVAL
     assert _create_status(tide, 2, [4], [4], out=False) == tide.TIDE_EINVAL
     assert _create_status(tide, 2, [1 << 40], [1 << 30]) == tide.TIDE_ERANGE
+    # unknown flags and contradictory copy-engine forms
+    assert _create_status(tide, 2, [4], [4], flags=0x100) == tide.TIDE_EINVAL
+    assert _create_status(tide, 2, [4], [4], flags=tide.TIDE_FLAG_CE_1D | tide.TIDE_FLAG_CE_2D) == tide.TIDE_EINVAL
+    assert _create_status(tide, 2, [4], [4], flags=tide.TIDE_FLAG_CE_1D | tide.TIDE_FLAG_CE_STRICT) == tide.TIDE_EINVAL
 
 
 def test_plan_layout_rejects(tide):
@@ -99,6 +103,7 @@ def test_null_group_calls(tide):
     assert L.tide_group_shard_elems(None, ctypes.byref(v)) == tide.TIDE_EINVAL
     k = ctypes.c_int32()
     assert L.tide_group_ag_kernel(None, ctypes.byref(k)) == tide.TIDE_EINVAL
+    assert L.tide_group_set_ce_bands(None, 2) == tide.TIDE_EINVAL
     assert L.tide_group_destroy(None) == tide.TIDE_OK
 
 
@@ -110,6 +115,11 @@ def test_probe_argument_checks_before_cuda(tide):
     assert L.tide_probe_bulk_read(None, 1024, 1, 4096, 4, None, None) == tide.TIDE_EINVAL
     assert L.tide_probe_bulk_read(16, 1024, 1, 4095, 4, 16, None) == tide.TIDE_EINVAL
     assert L.tide_probe_bulk_read(16, 1024, 1, 65536, 4, 16, None) == tide.TIDE_EINVAL  # > 200 KB staged
+    ok = dict(buf=256, bulk=1 << 20, ldg=1 << 20, ctas=16, copy=46080, stages=4, cons=8, ldgw=7, out=16)
+    for k, bad in (("buf", 0), ("buf", 272), ("ctas", 0), ("copy", 46081), ("stages", 17), ("stages", 5),
+                   ("cons", -1), ("ldgw", 8), ("ldg", 33), ("out", 0)):
+        args = dict(ok, **{k: bad})
+        assert L.tide_probe_ingest(*args.values(), None) == tide.TIDE_EINVAL, (k, bad)
 
 
 def test_pointer_table_marshalling(tide):

@@ -60,19 +60,40 @@ def test_byte_formulas_match_stated_sizes():
 def test_reference_arm_json_contract():
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
     res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
-                          "--warmup", "3", "--workload", "llama8b"], capture_output=True, text=True, env=env,
-                         timeout=900)
+                          "--warmup", "3", "--workload", "llama8b", "--scale", "8"], capture_output=True, text=True,
+                         env=env, timeout=900)
     assert res.returncode == 0, res.stderr
     line = json.loads(res.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["cpu_baseline"]["cores"] == len(os.sched_getaffinity(0))
     assert line["e2e"]["h2d_bytes_per_step"] == 0
-
-
-def test_all_cores_baseline_runs_one_replica_per_core():
+    # the reference arm processes exactly the GPU arm's workload: same config dict
     g = group("llama8b").scaled(8)
-    res = bench.cpu_baseline_all_cores(g, None, reps=2)
-    assert res["kind"] == "oracle" and res["unit"] == "GB/s" and res["value"] > 0
+    S, U = bench.layout(g)
+    assert line["config"] == json.loads(json.dumps(bench.workload_config(g, S, U, 1)))
+
+
+def test_host_oracle_baseline_covers_the_whole_group():
+    g = group("llama8b").scaled(8)
+    res = bench.cpu_baseline(g, None, passes=1)
+    assert res["kind"] == "oracle" and res["unit"] == "GB/s" and res["value"] > 0 and res["one_thread_gbs"] > 0
     assert res["cores"] == len(os.sched_getaffinity(0))
-    assert "k, v" in res["sample"] and res["cpu_model"]
+    assert "whole" in res["sample"] and res["cpu_model"]
+
+
+def test_host_oracle_parts_give_the_whole_group_result():
+    """The threaded host baseline computes exactly the oracle's whole-group outputs."""
+    import numpy as np
+
+    import oracle
+
+    g = group("qwen3moe").scaled(16)
+    ho = bench.HostOracle(g, None)
+    ho.time_passes(1, 0, 4)
+    want = oracle.reduce_scatter(ho.lay, ho.grads)
+    for d in range(g.R):
+        assert np.array_equal(ho.out[d].view(np.uint32), want[d].view(np.uint32))
+    params = oracle.all_gather(ho.lay, ho.shards, [np.zeros(g.numel(p), np.uint16) for p in range(g.P)])
+    for p in range(g.P):
+        assert np.array_equal(ho.params[p], params[p])

@@ -112,7 +112,7 @@ def run_rs(tide, g, ctas=0, misalign=False, flags=0, variant=0):
     G.close()
 
 
-def run_ag(tide, g, ce=False, ctas=0, misalign=False, uniform=True, flags=0, variant=0):
+def run_ag(tide, g, ce=False, ctas=0, misalign=False, uniform=True, flags=0, variant=0, bands=1):
     lay = oracle.plan(g.R, g.rows, g.row_len)
     host = []
     for r in range(g.R):
@@ -140,6 +140,7 @@ def run_ag(tide, g, ce=False, ctas=0, misalign=False, uniform=True, flags=0, var
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
     G.set_ctas(0, ctas)
     G.set_ag_variant(variant)
+    G.set_ce_bands(bands)
     if ce:
         G.all_gather_ce(shard_views, [x.view for x in params])
     else:
@@ -278,11 +279,70 @@ def test_all_gather_bulk_cta_counts(tide, ctas):
 
 @pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
 def test_all_gather_ce_matches_oracle(tide, g):
-    """Default copy-engine form: one 1-D copy per (rank, parameter) run of valid rows."""
-    copies, uniform = run_ag(tide, g, ce=True)
+    """1-D copy-engine form: one 1-D copy per (rank, parameter) run of valid rows."""
+    copies, uniform = run_ag(tide, g, ce=True, flags=tide.TIDE_FLAG_CE_1D)
     lay = oracle.plan(g.R, g.rows, g.row_len)
     assert not uniform
     assert copies == sum(1 for r in range(g.R) for p in range(g.P) if lay.valid_rows(r, p) > 0)
+
+
+def _ce_auto_expects_2d(g, lay):
+    """The default form rule restated: 2-D when the valid runs average under 8 MiB."""
+    runs = sum(1 for r in range(g.R) for p in range(g.P) if lay.valid_rows(r, p) > 0)
+    return 2 * lay.U < runs * (8 << 20)
+
+
+@pytest.mark.parametrize("g", [group("llama70b"), group("qwen3moe").scaled(4), group("tiny")],
+                         ids=["llama70b-full", "qwen3moe-div4", "tiny"])
+def test_all_gather_ce_default_form(tide, g):
+    """No form flag: the 2-D form for groups of short runs, the 1-D form for long runs (the full
+    Llama-3.1-70B layer); under TIDE_FLAG_OVERLAP always the 1-D form over one lane."""
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    if lay.U > (1 << 26):  # full-size group: the form choice only, through one unchecked call
+        G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+        shards = torch.zeros(g.R, lay.S, dtype=torch.int16, device="cuda")
+        params = [torch.empty(g.numel(p), dtype=torch.int16, device="cuda") for p in range(g.P)]
+        G.all_gather_ce(list(shards), params)
+        torch.cuda.synchronize()
+        assert G.last_ce_copies()[1] == int(_ce_auto_expects_2d(g, lay)) == 0
+        G.close()
+        del shards, params
+        torch.cuda.empty_cache()
+        return
+    copies, uniform = run_ag(tide, g, ce=True)
+    assert uniform == _ce_auto_expects_2d(g, lay)
+    copies, uniform = run_ag(tide, g, ce=True, flags=tide.TIDE_FLAG_OVERLAP)
+    assert not uniform
+
+
+def test_overlap_mode_defaults_and_parity(tide):
+    """TIDE_FLAG_OVERLAP: both SM kernels default to sm_count / 9 CTAs, the placement then takes
+    the bulk kernel, the copy-engine placement the 1-D form; every output matches the oracle."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    g = group("llama8b").scaled(16)
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_OVERLAP)
+    assert G.get_ctas() == (max(1, sms // 9), max(1, sms // 9))
+    assert G.ag_kernel() == tide.TIDE_AG_BULK
+    G.set_ctas(40, 24)
+    assert G.get_ctas() == (40, 24)
+    G.close()
+    for gg in (g, group("qwen3moe").scaled(16), edge_groups()[2]):
+        run_rs(tide, gg, flags=tide.TIDE_FLAG_OVERLAP)
+        run_ag(tide, gg, flags=tide.TIDE_FLAG_OVERLAP)
+        copies, uniform = run_ag(tide, gg, ce=True, flags=tide.TIDE_FLAG_OVERLAP)
+        assert not uniform
+
+
+@pytest.mark.parametrize("bands", [2, 3, 64])
+def test_all_gather_ce_2d_bands_match_oracle(tide, bands):
+    """Each parameter's strided copy split into bands of ranks: same bits, min(bands, f_p) 2-D
+    copies per parameter plus the partial rank's copy."""
+    for g in (group("wan_r16").scaled(8), group("qwen3moe").scaled(16), edge_groups()[1]):
+        copies, uniform = run_ag(tide, g, ce=True, flags=tide.TIDE_FLAG_CE_2D, bands=bands)
+        assert uniform
+        lay = oracle.plan(g.R, g.rows, g.row_len)
+        expect = sum(min(bands, r // int(m)) + (r % int(m) > 0) for r, m in zip(g.rows, lay.m))
+        assert copies == expect
 
 
 @pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))

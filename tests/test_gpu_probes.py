@@ -43,3 +43,29 @@ def test_bulk_read_probe_checksum(tide):
     got = out.cpu().numpy().view(np.uint32)
     assert got[1] == 0
     assert got[0] == want
+
+
+@pytest.mark.parametrize("consumers,ldg_warps", [(15, 0), (0, 0), (8, 7), (1, 14)])
+def test_ingest_probe_reads_every_byte(tide, consumers, ldg_warps):
+    """The per-SM ingest probe reads all of both parts: its checksum equals the XOR of every 32-bit
+    word of the bulk part (or of each copy's first word when the slots are not read out) and of
+    every word of the register-load part."""
+    copy, stages = 46080, 4
+    bulk = (96 << 20) // copy * copy if ldg_warps < 14 else 0
+    ldg = (32 << 20) if ldg_warps else 0
+    ldg_off = (bulk + 255) // 256 * 256
+    words = (ldg_off + ldg) // 4 + 64
+    buf = torch.randint(-2**31, 2**31 - 1, (words,), dtype=torch.int32, device="cuda")
+    out = torch.zeros(2, dtype=torch.int32, device="cuda")
+    tide.tide_probe_ingest(buf, bulk, ldg, 16, copy, stages, consumers, ldg_warps, out)
+    torch.cuda.synchronize()
+    h = buf.cpu().numpy().view(np.uint32)
+    want = np.uint32(0)
+    if bulk:
+        part = h[: bulk // 4]
+        want ^= np.bitwise_xor.reduce(part if consumers else part.reshape(-1, copy // 4)[:, 0])
+    if ldg:
+        want ^= np.bitwise_xor.reduce(h[ldg_off // 4: (ldg_off + ldg) // 4])
+    got = out.cpu().numpy().view(np.uint32)
+    assert got[1] == 0
+    assert got[0] == want
