@@ -313,7 +313,7 @@ int tide_probe_ingest(const void* buf, int64_t bulk_bytes, int64_t ldg_bytes, in
                       int32_t stages, int32_t consumer_warps, int32_t ldg_warps, uint32_t* out, void* stream) {
     const int consumers = consumer_warps > 0 ? consumer_warps : 1;
     if (!buf || !out || bulk_bytes < 0 || ldg_bytes < 0 || ctas < 1 || copy_bytes < 16 || copy_bytes % 16 ||
-        stages < 1 || stages > 16 || int64_t(copy_bytes) * stages > 220 * 1024 || consumer_warps < 0 ||
+        stages < 1 || stages > 16 || 256 + int64_t(copy_bytes) * stages > int64_t(tide::kMaxDynamicSmem) || consumer_warps < 0 ||
         ldg_warps < 0 || 1 + consumers + ldg_warps > 16 || (reinterpret_cast<uintptr_t>(buf) & 255u) ||
         ldg_bytes % 32)
         return TIDE_EINVAL;

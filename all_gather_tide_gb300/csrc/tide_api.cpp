@@ -247,15 +247,15 @@ bool ag_uses_bulk(const tide_group* g, bool aligned) {
 // pointers (the register path's element-wise fallback covers the rest).  Measured on GB300 it is the faster of
 // the two at every CTA count, most of all when the count is capped below the SM count.
 // Copy-engine form when the caller fixes none (neither TIDE_FLAG_CE_1D nor TIDE_FLAG_CE_2D): the
-// host spends about 2 us submitting each copy, so the 1-D form (one copy per (rank, parameter)
-// run, up to 6.4 TB/s over 8 lanes) is host-bound when runs are short, while the 2-D form (one
-// strided copy per parameter) holds ~3.5 TB/s on every workload measured on GB300.  The 1-D form
-// wins while runs average >= 8 MiB (Llama-3.1-70B layer 48 MB: 6.5 against 3.7 TB/s; 8B layer
-// 12 MB: 5.0 against 3.6; Wan R = 8, 11 MB: 3.8 against 3.5), the 2-D form below (Wan R = 16,
-// 5.6 MB: 3.5 against 2.5; Qwen3 MoE layer, 0.8 MB: 2.6 against 0.37).  Under TIDE_FLAG_OVERLAP
-// the 1-D form over one lane is kept whatever the run length: strided copies slowed a concurrent
-// GEMM far more per byte (+149 % against +4 % on the 70B layer).
-constexpr int64_t kCe1dMinAvgRunBytes = int64_t(8) << 20;
+// host spends one to two microseconds submitting each copy, so the 1-D form (one copy per (rank,
+// parameter) run, up to 6.4 TB/s over 8 lanes) is host-bound when runs are short, while the 2-D
+// form (one strided copy per parameter) holds ~3.5 TB/s on every workload measured on GB300.  The
+// 1-D form wins while runs average >= 4 MiB (Llama-3.1-70B layer, 24 MB runs: 6.5 against
+// 3.7 TB/s; 8B layer, 6 MB: 5.0 against 3.6; Wan R = 8, 5.6 MB: 3.8 against 3.5), the 2-D form
+// below (Wan R = 16, 2.8 MB: 3.6 against 2.5; Qwen3 MoE layer, 0.4 MB: 2.6 against 0.37).  Under
+// TIDE_FLAG_OVERLAP the 1-D form over one lane is kept whatever the run length: strided copies
+// slowed a concurrent GEMM far more per byte (+149 % against +4 % on the 70B layer).
+constexpr int64_t kCe1dMinAvgRunBytes = int64_t(4) << 20;
 
 bool ce_auto_prefers_2d(const tide_group* g) {
     if (g->flags & TIDE_FLAG_OVERLAP) return false;

@@ -309,6 +309,11 @@ def run_tide(args, rank, world, local_rank):
     if args.ce_lanes:
         G1.set_ce_lanes(args.ce_lanes)
     legs["all_gather_ce_2d"] = time_ce(G1, buf, stream, b_ag, max(3, args.steps))
+    # each parameter's strided copy split into bands of ranks, spread over the lanes
+    for bands in args.ce_bands_sweep:
+        G1.set_ce_bands(bands)
+        legs[f"all_gather_ce_2d_bands{bands}"] = time_ce(G1, buf, stream, b_ag, max(3, args.steps))
+    G1.set_ce_bands(1)
     for lanes in args.ce_lanes_sweep:
         for name, grp in (("1d", G), ("2d", G1)):
             grp.set_ce_lanes(lanes)
@@ -1161,6 +1166,7 @@ def main():
     ap.add_argument("--ag-variant", choices=["auto", "register", "bulk"], default="auto")
     ap.add_argument("--ce-lanes", type=int, default=0, help="copy-engine streams (0 = library default)")
     ap.add_argument("--ce-lanes-sweep", type=int, nargs="*", default=[])
+    ap.add_argument("--ce-bands-sweep", type=int, nargs="*", default=[2, 4, 8])
     ap.add_argument("--interference-ctas", type=int, nargs="*", default=[8, 12, 16, 20, 24, 32])
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-passes", type=int, default=3, help="whole-group oracle passes of the CPU baseline")

@@ -177,7 +177,7 @@ int tide_all_gather(tide_group_t g, const void *const *shards, void *const *para
  *     partial piece.  ~3.5 TB/s on every workload measured, 2.6 TB/s on the Qwen3 MoE layer.
  * TIDE_FLAG_CE_1D or TIDE_FLAG_CE_2D fixes the form (TIDE_FLAG_CE_2D falls back to 1-D without a
  * uniform pitch, or returns TIDE_ELAYOUT under TIDE_FLAG_CE_STRICT).  With neither flag the group
- * takes the 2-D form when the pitch is uniform and its runs average less than 8 MiB, else the 1-D
+ * takes the 2-D form when the pitch is uniform and its runs average less than 4 MiB, else the 1-D
  * form; under TIDE_FLAG_OVERLAP always the 1-D form (the strided copies slow a concurrent GEMM far
  * more per byte moved).
  */
@@ -334,7 +334,7 @@ int tide_probe_bulk_read(const void *buf, int64_t bytes, int32_t ctas, int32_t c
  * (each claims copy_bytes*stages of shared memory, so one per SM) read the device buffer `buf`
  * (256-byte aligned) in two parts at once:
  *   - [buf, buf + bulk_bytes): bulk copies of `copy_bytes` (multiple of 16) through `stages`
- *     shared-memory slots (copy_bytes*stages <= 220 KB, stages <= 16), each landed slot read out by
+ *     shared-memory slots (copy_bytes*stages <= 231168 bytes, stages <= 16), each landed slot read out by
  *     `consumer_warps` warps, every 16-byte word (0: only its first word, the copy engine alone);
  *     whole copies only (bulk_bytes / copy_bytes of them);
  *   - the next ldg_bytes (a multiple of 32) from buf + round_up(bulk_bytes, 256): `ldg_warps` warps

@@ -116,7 +116,7 @@ def test_probe_argument_checks_before_cuda(tide):
     assert L.tide_probe_bulk_read(16, 1024, 1, 4095, 4, 16, None) == tide.TIDE_EINVAL
     assert L.tide_probe_bulk_read(16, 1024, 1, 65536, 4, 16, None) == tide.TIDE_EINVAL  # > 200 KB staged
     ok = dict(buf=256, bulk=1 << 20, ldg=1 << 20, ctas=16, copy=46080, stages=4, cons=8, ldgw=7, out=16)
-    for k, bad in (("buf", 0), ("buf", 272), ("ctas", 0), ("copy", 46081), ("stages", 17), ("stages", 5),
+    for k, bad in (("buf", 0), ("buf", 272), ("ctas", 0), ("copy", 46081), ("stages", 17), ("stages", 6),
                    ("cons", -1), ("ldgw", 8), ("ldg", 33), ("out", 0)):
         args = dict(ok, **{k: bad})
         assert L.tide_probe_ingest(*args.values(), None) == tide.TIDE_EINVAL, (k, bad)

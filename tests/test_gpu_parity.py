@@ -287,9 +287,9 @@ def test_all_gather_ce_matches_oracle(tide, g):
 
 
 def _ce_auto_expects_2d(g, lay):
-    """The default form rule restated: 2-D when the valid runs average under 8 MiB."""
+    """The default form rule restated: 2-D when the valid runs average under 4 MiB."""
     runs = sum(1 for r in range(g.R) for p in range(g.P) if lay.valid_rows(r, p) > 0)
-    return 2 * lay.U < runs * (8 << 20)
+    return 2 * lay.U < runs * (4 << 20)
 
 
 @pytest.mark.parametrize("g", [group("llama70b"), group("qwen3moe").scaled(4), group("tiny")],
