@@ -308,6 +308,7 @@ def run_tide(args, rank, world, local_rank):
     G1 = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_CE_2D)
     if args.ce_lanes:
         G1.set_ce_lanes(args.ce_lanes)
+    G1.set_ce_bands(1)  # the paper's form: one strided copy per parameter
     legs["all_gather_ce_2d"] = time_ce(G1, buf, stream, b_ag, max(3, args.steps))
     # each parameter's strided copy split into bands of ranks, spread over the lanes
     for bands in args.ce_bands_sweep:
@@ -631,8 +632,9 @@ def interference(G, buf, stream, dev, args):
     if "operating_point" in out:
         out["operating_point"]["bound_16_sms_gbs"] = bound
         out["operating_point"]["bound_16_sms_frac"] = bound / peak
-        out["operating_point"]["bound_rule"] = ("16 x the measured per-SM ingest ceiling x (algorithmic bytes / "
-                                                "bytes read): no kernel on 16 SMs can exceed it")
+        out["operating_point"]["bound_rule"] = ("16 x the most bytes per second any ingest-probe mode brought into "
+                                                "one SM x (algorithmic bytes / bytes read): the reduce-scatter must "
+                                                "bring its inputs into the SMs that run it")
     # the placement is short; run it several times back to back so GEMMs fit inside
     out["all_gather_sm"] = dict(ctas=ag_default, **concurrent(
         lambda: [G.all_gather(buf.ag_list, buf.params, stream) for _ in range(8)], "ag"))
@@ -754,6 +756,7 @@ def cta_sweep(G, buf, stream, args, concurrent):
     # copy-engine placement: no SM is taken, so the only knob is how many copies run at once
     # (the streams they are spread over); HBM and L2 contention is what slows the GEMM
     G2 = tide.Group(G.R, list(zip(G.rows, G.row_len)), tide.TIDE_FLAG_CE_2D)
+    G2.set_ce_bands(1)  # the paper's form: one strided copy per parameter
     for form, grp in (("1d", G), ("2d", G2)):
         for lanes in (1, 2, 4, 8):
             grp.set_ce_lanes(lanes)
@@ -854,6 +857,17 @@ def probes(G, buf, stream, dev, args):
                       "slowdown_pct": 100 * (statistics.median(inside) / t_alone["gemm_1wave_4096x4096x8192"] - 1)
                       if inside else None})
     out["spin_curve"] = curve
+    # the same resident CTAs launched as clusters: does packing them into whole cluster slots leave
+    # the GEMM more room?
+    clustered = []
+    for cl in (2, 4, 8):
+        for n in (16, 20, 24, 32):
+            hold = lambda: tide.tide_probe_hold(n, 1024, 213 * 1024, cl, 20_000_000, None, stream)
+            _, inside = _window_times(hold, vs, g1, 64, stream)
+            clustered.append({"cluster": cl, "resident_ctas": n, "gemms": len(inside),
+                              "slowdown_pct": 100 * (statistics.median(inside) / t_alone["gemm_1wave_4096x4096x8192"] - 1)
+                              if inside else None})
+    out["spin_curve_clustered"] = clustered
 
     # Table 4 / Table 5 for several reduce-scatter configurations, and for the copy-engine
     # placement (8 placements back to back, so the victims and probes overlap it)
@@ -861,6 +875,7 @@ def probes(G, buf, stream, dev, args):
                ("reduce_scatter", "register", 16), ("all_gather_ce", "1d", 1), ("all_gather_ce", "1d", 8),
                ("all_gather_ce", "2d", 1)]
     G2 = tide.Group(G.R, list(zip(G.rows, G.row_len)), tide.TIDE_FLAG_CE_2D)
+    G2.set_ce_bands(1)  # the paper's form: one strided copy per parameter
     rows = []
     recs = torch.zeros(3 * sms, dtype=torch.int64, device=dev)
     for coll, variant, n_ in configs:
