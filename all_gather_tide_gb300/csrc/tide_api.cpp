@@ -73,7 +73,7 @@ struct tide_group {
     // copy-engine work is spread over `ce_lanes` streams forked from and joined back to the
     // caller's stream, so several copy engines run at once
     int ce_lanes = kMaxCeLanes;  // measured on GB300: 1-D copies over 8 streams reach ~0.94 x HBM peak
-    int ce_bands = 0;  // 2-D copies per parameter (bands of ranks); 0 = chosen by run length
+    int ce_bands = 1;  // 2-D copies per parameter (bands of ranks)
     cudaStream_t lane_stream[kMaxCeLanes] = {};
     cudaEvent_t lane_done[kMaxCeLanes] = {};
     cudaEvent_t fork = nullptr;
@@ -247,32 +247,21 @@ bool ag_uses_bulk(const tide_group* g, bool aligned) {
 // pointers (the register path's element-wise fallback covers the rest).  Measured on GB300 it is the faster of
 // the two at every CTA count, most of all when the count is capped below the SM count.
 // Copy-engine form when the caller fixes none (neither TIDE_FLAG_CE_1D nor TIDE_FLAG_CE_2D): the
-// 2-D form whenever the shards sit at a uniform pitch, with the bands chosen by run length, else
-// the 1-D form.  The host spends one to two microseconds submitting each copy, and the copy
-// engines move many long copies at once faster than a few; measured on GB300 (8 lanes):
-//   - runs averaging >= 4 MiB: 2-D copies split into one band of ranks per lane match or beat
-//     one 1-D copy per run (Llama-3.1-70B layer, 24 MB runs: 6.45 against 6.45 TB/s; 8B layer,
-//     6 MB: 5.15 against 4.98; Wan R = 8, 5.6 MB: 4.16 against 3.69), while one strided copy per
-//     parameter reaches only 3.5-3.7;
-//   - shorter runs: one strided copy per parameter (Wan R = 16, 2.8 MB runs: 3.55 against 2.5 for
-//     1-D; Qwen3 MoE layer, 0.4 MB: 2.6 against 0.37), where splitting into bands only adds copies
-//     (Qwen3: 0.38 TB/s with 8 bands).
-// Under TIDE_FLAG_OVERLAP the 1-D form over one lane is kept whatever the run length: strided
-// copies slowed a concurrent GEMM far more per byte (+149 % against +4 % on the 70B layer).
+// host spends one to two microseconds submitting each copy, so the 1-D form (one copy per (rank,
+// parameter) run, up to 6.4 TB/s over 8 lanes, 4.5 over one) is host-bound when runs are short,
+// while one strided 2-D copy per parameter holds ~3.5 TB/s on every workload measured on GB300.
+// The 1-D form wins while runs average >= 4 MiB (Llama-3.1-70B layer, 24 MB runs: 6.5 against
+// 3.7 TB/s; 8B layer, 6 MB: 5.0 against 3.6; Wan R = 8, 5.6 MB: 3.7 against 3.5), the 2-D form below
+// (Wan R = 16, 2.8 MB runs: 3.5 against 2.5; Qwen3 MoE layer, 0.4 MB: 2.6 against 0.37).  The 1-D
+// form is also the one that stays gentle on concurrent compute over few lanes (one lane: +4-7 % on a
+// single-wave GEMM against +142-149 % for strided copies on the 70B layer), so it is kept under
+// TIDE_FLAG_OVERLAP whatever the run length.
 constexpr int64_t kCeLongRunBytes = int64_t(4) << 20;
 
-bool ce_auto_prefers_2d(const tide_group* g) { return !(g->flags & TIDE_FLAG_OVERLAP); }
-
-bool ce_long_runs(const tide_group* g) {
+bool ce_auto_prefers_2d(const tide_group* g) {
+    if (g->flags & TIDE_FLAG_OVERLAP) return false;
     const int64_t runs = int64_t(g->plan.ag.size());
-    return runs > 0 && 2 * g->plan.U >= runs * kCeLongRunBytes;
-}
-
-// 2-D copies per parameter: as set, or (0, the default) one band per lane for long runs, one
-// strided copy per parameter otherwise.
-int64_t ce_bands(const tide_group* g) {
-    if (g->ce_bands > 0) return g->ce_bands;
-    return ce_long_runs(g) ? g->ce_lanes : 1;
+    return runs > 0 && 2 * g->plan.U < runs * kCeLongRunBytes;
 }
 
 bool use_bulk(const tide_group* g, bool aligned) {
@@ -556,7 +545,7 @@ int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* p
             // by default: the whole parameter in one strided copy), source rows `pitch` apart,
             // destination rows contiguous
             const int64_t f = pl.rows[p] / pl.m[p];
-            const int64_t nb = std::min<int64_t>(ce_bands(g), f);
+            const int64_t nb = std::min<int64_t>(g->ce_bands, f);
             for (int64_t b = 0; b < nb; ++b) {
                 const int64_t r0 = f * b / nb, r1 = f * (b + 1) / nb;
                 TIDE_CUDA(cudaMemcpy2DAsync(dst + r0 * piece_bytes, size_t(piece_bytes),
@@ -611,7 +600,7 @@ int tide_group_set_ce_lanes(tide_group_t g, int32_t lanes) {
 }
 
 int tide_group_set_ce_bands(tide_group_t g, int32_t bands) {
-    if (!g || bands < 0 || bands > TIDE_MAX_RANKS) return TIDE_EINVAL;
+    if (!g || bands < 1 || bands > TIDE_MAX_RANKS) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);
     g->ce_bands = bands;
     return TIDE_OK;

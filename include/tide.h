@@ -177,11 +177,9 @@ int tide_all_gather(tide_group_t g, const void *const *shards, void *const *para
  *     partial piece.  ~3.5 TB/s on every workload measured, 2.6 TB/s on the Qwen3 MoE layer.
  * TIDE_FLAG_CE_1D or TIDE_FLAG_CE_2D fixes the form (TIDE_FLAG_CE_2D falls back to 1-D without a
  * uniform pitch, or returns TIDE_ELAYOUT under TIDE_FLAG_CE_STRICT).  With neither flag the group
- * takes the 2-D form whenever the pitch is uniform, else the 1-D form; under TIDE_FLAG_OVERLAP
- * always the 1-D form (the strided copies slow a concurrent GEMM far more per byte moved).  By
- * default (tide_group_set_ce_bands) a group whose valid runs average at least 4 MiB splits each
- * 2-D copy into one band of ranks per lane (Llama-3.1-70B layer: 6.45 TB/s, as fast as the 1-D
- * form; 8B layer: 5.15 against 4.98 TB/s), and any other group keeps one strided copy per parameter.
+ * takes the 2-D form when the pitch is uniform and its valid runs average less than 4 MiB, else the
+ * 1-D form; under TIDE_FLAG_OVERLAP always the 1-D form (strided copies slow a concurrent GEMM far
+ * more per byte moved: +142-149 % against +4-7 % over one lane on the Llama-3.1-70B layer).
  */
 int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *params,
                        void *stream);
@@ -267,9 +265,10 @@ int tide_group_set_ce_lanes(tide_group_t g, int32_t lanes);
 /*
  * Splits each parameter's 2-D copy (the uniform-pitch form of tide_all_gather_ce) into up to
  * `bands` 2-D copies over consecutive bands of ranks, spread over the copy-engine lanes like the
- * 1-D copies (1..TIDE_MAX_RANKS; 1 = the paper's single strided copy per parameter).  0 (the
- * default) chooses by run length: one band per lane when the group's valid runs average at least
- * 4 MiB, else one strided copy per parameter.
+ * 1-D copies (1..TIDE_MAX_RANKS, default 1: the paper's single strided copy per parameter).  Measured
+ * on GB300 over 8 lanes: one band per lane runs as fast as the 1-D form on long-run groups
+ * (Llama-3.1-70B layer 6.45 TB/s; 8B layer 5.2 against 5.0) but slows groups of many parameters
+ * (Qwen3 MoE layer: 0.39 against 2.6 TB/s with one band).
  */
 int tide_group_set_ce_bands(tide_group_t g, int32_t bands);
 

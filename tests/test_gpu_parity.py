@@ -286,38 +286,32 @@ def test_all_gather_ce_matches_oracle(tide, g):
     assert copies == sum(1 for r in range(g.R) for p in range(g.P) if lay.valid_rows(r, p) > 0)
 
 
-def _ce_auto_bands(g, lay, lanes=8):
-    """The default band rule restated: one band per lane when the valid runs average >= 4 MiB."""
+def _ce_auto_expects_2d(g, lay):
+    """The default form rule restated: 2-D when the valid runs average under 4 MiB."""
     runs = sum(1 for r in range(g.R) for p in range(g.P) if lay.valid_rows(r, p) > 0)
-    return lanes if 2 * lay.U >= runs * (4 << 20) else 1
-
-
-def _ce_2d_copies(g, lay, bands):
-    return sum(min(bands, r // int(m)) + (r % int(m) > 0) for r, m in zip(g.rows, lay.m))
+    return 2 * lay.U < runs * (4 << 20)
 
 
 @pytest.mark.parametrize("g", [group("llama70b"), group("qwen3moe").scaled(4), group("tiny")],
                          ids=["llama70b-full", "qwen3moe-div4", "tiny"])
 def test_all_gather_ce_default_form(tide, g):
-    """No form flag and a uniform pitch: the 2-D form, one band per lane for long runs (the full
-    Llama-3.1-70B layer) and one strided copy per parameter otherwise; under TIDE_FLAG_OVERLAP
-    always the 1-D form over one lane."""
+    """No form flag and a uniform pitch: the 2-D form for groups of short runs, the 1-D form for long
+    runs (the full Llama-3.1-70B layer); under TIDE_FLAG_OVERLAP always the 1-D form over one lane."""
     lay = oracle.plan(g.R, g.rows, g.row_len)
-    want = _ce_2d_copies(g, lay, _ce_auto_bands(g, lay))
-    if lay.U > (1 << 26):  # full-size group: the form and copy count only, through one unchecked call
+    if lay.U > (1 << 26):  # full-size group: the form choice only, through one unchecked call
         G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
         shards = torch.zeros(g.R, lay.S, dtype=torch.int16, device="cuda")
         params = [torch.empty(g.numel(p), dtype=torch.int16, device="cuda") for p in range(g.P)]
         G.all_gather_ce(list(shards), params)
         torch.cuda.synchronize()
-        assert G.last_ce_copies() == (want, 1) and _ce_auto_bands(g, lay) == 8
+        assert G.last_ce_copies()[1] == int(_ce_auto_expects_2d(g, lay)) == 0
         G.close()
         del shards, params
         torch.cuda.empty_cache()
         return
-    copies, uniform = run_ag(tide, g, ce=True, bands=0)
-    assert uniform and copies == want
-    copies, uniform = run_ag(tide, g, ce=True, flags=tide.TIDE_FLAG_OVERLAP, bands=0)
+    copies, uniform = run_ag(tide, g, ce=True)
+    assert uniform == _ce_auto_expects_2d(g, lay)
+    copies, uniform = run_ag(tide, g, ce=True, flags=tide.TIDE_FLAG_OVERLAP)
     assert not uniform
 
 
