@@ -862,6 +862,8 @@ def probes(G, buf, stream, dev, args):
     clustered = []
     for cl in (2, 4, 8):
         for n in (16, 20, 24, 32):
+            if n % cl:
+                continue  # whole clusters only
             hold = lambda: tide.tide_probe_hold(n, 1024, 213 * 1024, cl, 20_000_000, None, stream)
             _, inside = _window_times(hold, vs, g1, 64, stream)
             clustered.append({"cluster": cl, "resident_ctas": n, "gemms": len(inside),
