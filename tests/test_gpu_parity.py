@@ -439,6 +439,18 @@ def test_random_groups(tide):
         run_ag(tide, g, ce=True)
 
 
+@pytest.mark.parametrize("R", [1024, 4096])
+def test_many_ranks(tide, R):
+    """Rank counts up to the library's maximum (TIDE_MAX_RANKS): the bulk reduce-scatter's per-piece
+    pointer cache grows to 8 R bytes and leaves room for fewer stages; most ranks hold no rows of the
+    short parameter, and odd piece offsets mix bulk copies and element-wise sums."""
+    g = Group(f"many-ranks-R{R}", R, (("a", 2 * R, 8), ("b", R + R // 2 - 36, 16), ("c", 7, 4)))
+    run_rs(tide, g)
+    run_rs(tide, g, ctas=16)
+    run_ag(tide, g)
+    run_ag(tide, g, ce=True)
+
+
 def test_pointer_table_ring_and_streams(tide):
     """Alternating buffer sets and streams reuse or refill the pointer-table ring correctly."""
     g = group("llama70b").scaled(64)
