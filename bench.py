@@ -357,6 +357,10 @@ def run_tide(args, rank, world, local_rank):
                        "algorithmic_bytes": b_rs}
     out["clocks"] = clocks.summary()
 
+    # end to end first, while nothing but the step has run on the device and the host link
+    if not args.no_e2e:
+        out["e2e"] = end_to_end(G, g, buf, S, U, dev, args, world)
+        out["e2e"]["host_affinity"] = numa
     if args.slot_reuse and rank == 0:
         out["slot_reuse"] = slot_reuse(G, g, buf, S, U, stream)
     if not args.no_stock and rank == 0:
@@ -365,9 +369,6 @@ def run_tide(args, rank, world, local_rank):
         out["interference"] = interference(G, buf, stream, dev, args)
     if args.probes and rank == 0:
         out["probes"] = probes(G, buf, stream, dev, args)
-    if not args.no_e2e:
-        out["e2e"] = end_to_end(G, g, buf, S, U, dev, args, world)
-        out["e2e"]["host_affinity"] = numa
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(g, dev, passes=args.cpu_passes)
     G.close()
@@ -1033,7 +1034,13 @@ def end_to_end(G, g, buf, S, U, dev, args, world):
     ms = sorted(windows)[1]
     value = whole_job_gbs(rs_bytes(g, S, U) + ag_bytes(U), steps, world, ms)
     link = {"h2d_gbs_inputs_only": one_direction("h2d"), "d2h_gbs_same_bytes": one_direction("d2h")}
-    del h_grads, h_ag, h_shards, h_params
+    # the step cannot be shorter than its input copies over the host link alone
+    h2d_ms = h2d / (link["h2d_gbs_inputs_only"] * 1e9) * 1e3
+    link["h2d_bound_ms_per_step"] = h2d_ms
+    link["frac_of_h2d_bound"] = h2d_ms / (ms / steps)
+    del h_grads, h_ag, h_shards, h_params, pairs_in, pairs_out, lanes
+    if hasattr(torch._C, "_host_emptyCache"):  # hand the 20 GB of pinned buffers back to the host
+        torch._C._host_emptyCache()
     return {"value": value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": ms / steps, "host_link": link,
             "windows_gbs": [whole_job_gbs(rs_bytes(g, S, U) + ag_bytes(U), steps, world, w) for w in windows],
