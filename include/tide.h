@@ -296,7 +296,7 @@ int tide_group_last_ce_copies(tide_group_t g, int64_t *copies, int32_t *uniform_
  *     tables do not fit in TIDE_NOALLOC_SCRATCH_BYTES (e.g. R = 8 with P > 2047) is rejected
  *     with TIDE_ERANGE before anything is enqueued.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- *     that device current; make that first call before any stream capture.
+ *     that device current, once; later calls on that device reuse it.
  *   - Every call shares the one array, which keeps the last call's tables; nothing in it has to
  *     start at zero, because each call rewrites everything its kernel reads.  Calls on the same
  *     stream are ordered; calls that overlap on the GPU (different streams, or several host
