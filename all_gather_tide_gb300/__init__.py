@@ -57,6 +57,7 @@ SIGNATURES = {
     "tide_group_set_ctas": (ctypes.c_int, [_vp, ctypes.c_int32, ctypes.c_int32]),
     "tide_group_get_ctas": (ctypes.c_int, [_vp, _i32p, _i32p]),
     "tide_reduce_scatter": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
+    "tide_reduce_scatter_slots": (ctypes.c_int, [_vp, ctypes.c_int32, _vpp, _vp, _vp]),
     "tide_all_gather": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_all_gather_ce": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_group_last_ce_copies": (ctypes.c_int, [_vp, _i64p, _i32p]),
@@ -230,6 +231,13 @@ def tide_reduce_scatter(g: int, grads, shards: Sequence, stream=None) -> None:
            "tide_reduce_scatter")
 
 
+def tide_reduce_scatter_slots(g: int, d: int, slots: Sequence, shard, stream=None) -> None:
+    """``slots``: R bf16 staging slots of S elements (slot r holds contributor r's slice d of every
+    parameter at o_p); ``shard``: d's fp32 shard of S elements."""
+    _check(lib().tide_reduce_scatter_slots(g, d, _ptr_array(slots), _ptr(shard), _stream(stream)),
+           "tide_reduce_scatter_slots")
+
+
 def tide_all_gather(g: int, shards: Sequence, params: Sequence, stream=None) -> None:
     _check(lib().tide_all_gather(g, _ptr_array(shards), _ptr_array(params), _stream(stream)), "tide_all_gather")
 
@@ -369,6 +377,9 @@ class Group:
 
     def reduce_scatter(self, grads, shards, stream=None) -> None:
         tide_reduce_scatter(self.handle, grads, shards, stream)
+
+    def reduce_scatter_slots(self, d: int, slots, shard, stream=None) -> None:
+        tide_reduce_scatter_slots(self.handle, d, slots, shard, stream)
 
     def all_gather(self, shards, params, stream=None) -> None:
         tide_all_gather(self.handle, shards, params, stream)

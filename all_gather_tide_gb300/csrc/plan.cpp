@@ -91,6 +91,34 @@ void make_work_lists(Plan* pl) {
     }
     pl->rs_bulk_chunks = chunks;
 
+    // Summing step over staging slots: slot r of destination d holds contributor r's slice d of
+    // parameter p at o_p, so a piece reads every slot at o_p; chunk ranges count from 0 for each d.
+    pl->rs_slots.clear();
+    pl->rs_slot_piece.clear();
+    std::vector<int64_t> first(size_t(pl->P));
+    chunks = 0;
+    for (int32_t p = 0; p < pl->P; ++p) {
+        first[size_t(p)] = chunks;
+        const int64_t n = (pl->s[p] + kBulkChunk - 1) / kBulkChunk;
+        chunks += n;
+        pl->rs_slot_piece.insert(pl->rs_slot_piece.end(), size_t(n), p);
+    }
+    pl->rs_slot_chunks = chunks;
+    for (int32_t d = 0; d < pl->R; ++d) {
+        for (int32_t p = 0; p < pl->P; ++p) {
+            RsSeg sg{};
+            sg.dst_off = pl->o[p];
+            sg.src_off = pl->o[p];
+            sg.valid = valid_rows(pl->rows[p], pl->m[p], d) * pl->row_len[p];
+            sg.total = pl->s[p];
+            sg.chunk_begin = first[size_t(p)];
+            sg.d = 0;
+            sg.p = 0;
+            sg.vec = sg.src_off % 8 == 0;
+            pl->rs_slots.push_back(sg);
+        }
+    }
+
     // All-gather placement: source-rank-major runs of valid elements; padding never appears.
     pl->ag.clear();
     pl->ag_run.clear();

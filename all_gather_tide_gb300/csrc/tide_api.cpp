@@ -62,6 +62,8 @@ struct tide_group {
     int32_t* d_rs_piece = nullptr;  // piece index of every register-path chunk
     tide::RsSeg* d_rs_bulk = nullptr;
     int32_t* d_rs_bulk_piece = nullptr;  // piece index of every bulk chunk
+    tide::RsSeg* d_rs_slots = nullptr;      // pieces of the summing step over staging slots
+    int32_t* d_rs_slot_piece = nullptr;     // piece (0..P-1) of every chunk of one destination
     tide::AgSeg* d_ag_bulk = nullptr;
     tide::AgSeg* d_ag = nullptr;
     int32_t* d_ag_run = nullptr;  // run index of every register-path placement chunk
@@ -104,6 +106,8 @@ void release(tide_group* g) {
     if (g->d_rs_piece) cudaFree(g->d_rs_piece);
     if (g->d_rs_bulk) cudaFree(g->d_rs_bulk);
     if (g->d_rs_bulk_piece) cudaFree(g->d_rs_bulk_piece);
+    if (g->d_rs_slots) cudaFree(g->d_rs_slots);
+    if (g->d_rs_slot_piece) cudaFree(g->d_rs_slot_piece);
     if (g->d_ag_bulk) cudaFree(g->d_ag_bulk);
     if (g->d_status) cudaFree(g->d_status);
     if (g->d_ag) cudaFree(g->d_ag);
@@ -362,6 +366,16 @@ int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* ro
         if (e == cudaSuccess)
             e = cudaMemcpy(g->d_rs_bulk_piece, rp.data(), rp.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
     }
+    const auto& sl = g->plan.rs_slots;
+    const auto& slp = g->plan.rs_slot_piece;
+    if (e == cudaSuccess && !sl.empty() && !slp.empty()) {
+        e = cudaMalloc(&g->d_rs_slots, sl.size() * sizeof(tide::RsSeg));
+        if (e == cudaSuccess)
+            e = cudaMemcpy(g->d_rs_slots, sl.data(), sl.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
+        if (e == cudaSuccess) e = cudaMalloc(&g->d_rs_slot_piece, slp.size() * sizeof(int32_t));
+        if (e == cudaSuccess)
+            e = cudaMemcpy(g->d_rs_slot_piece, slp.data(), slp.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+    }
     const auto& ab = g->plan.ag_bulk;
     if (e == cudaSuccess && !ab.empty()) {
         e = cudaMalloc(&g->d_ag_bulk, ab.size() * sizeof(tide::AgSeg));
@@ -470,6 +484,39 @@ int tide_reduce_scatter(tide_group_t g, const void* const* grads, void* const* s
         e = tide::launch_reduce_scatter(g->d_rs, int(g->plan.rs.size()), g->d_rs_piece, g->plan.rs_chunks, gp, sp,
                                         R, P, aligned ? 1 : 0, ctas, st);
     }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return finish_slot(g, k, st);
+}
+
+int tide_reduce_scatter_slots(tide_group_t g, int32_t d, const void* const* slots, void* shard, void* stream) {
+    if (!g || !slots || !shard) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    const int R = g->plan.R, P = g->plan.P;
+    if (d < 0 || d >= R || !elem_aligned(shard, 4)) return TIDE_EINVAL;
+    std::vector<const void*> table(size_t(R) + 1);
+    bool aligned = true;
+    for (int r = 0; r < R; ++r) {
+        if (!slots[r] || !elem_aligned(slots[r], 2)) return TIDE_EINVAL;
+        table[size_t(r)] = slots[r];
+        aligned &= aligned16(slots[r]);
+    }
+    table[size_t(R)] = shard;
+    if (!aligned && (g->flags & TIDE_FLAG_VEC_STRICT)) return TIDE_EALIGN;
+    if (!g->d_rs_slots || !g->d_rs_slot_piece) return TIDE_EINVAL;
+    int rc = check_device(g);
+    if (rc != TIDE_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int k = 0;
+    if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
+    void** dev = g->slots[k].dev;
+    // one table entry per slot and one shard: the pieces carry p = 0 and d = 0
+    const auto* gp = reinterpret_cast<const uint16_t* const*>(dev);
+    auto* sp = reinterpret_cast<float* const*>(dev + R);
+    const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, true);
+    cudaError_t e = tide::launch_reduce_scatter_bulk(g->d_rs_slots + size_t(d) * size_t(P), g->d_rs_slot_piece,
+                                                     g->plan.rs_slot_chunks, gp, sp, R, 1, aligned ? 1 : 0, ctas,
+                                                     g->d_status, g->timeout_ns,
+                                                     (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return finish_slot(g, k, st);
 }

@@ -81,6 +81,13 @@ struct Plan {
     std::vector<RsSeg> rs_bulk;  // same pieces, chunked for the bulk-copy kernel
     int64_t rs_bulk_chunks = 0;
     std::vector<int32_t> rs_bulk_piece;  // index in rs_bulk of every bulk chunk's piece
+    // Summing step over staging slots (tide_reduce_scatter_slots): destination d's P pieces are
+    // rs_slots[d*P .. d*P + P), each reading slot r at o_p (one table entry per slot: p field 0)
+    // and writing the call's one shard (d field 0); their chunks, counted from 0 for every d, are
+    // the same for all destinations (only the valid counts differ).
+    std::vector<RsSeg> rs_slots;
+    int64_t rs_slot_chunks = 0;          // bulk chunks of one destination
+    std::vector<int32_t> rs_slot_piece;  // piece (0..P-1) of each of those chunks
     std::vector<AgSeg> ag;
     int64_t ag_chunks = 0;
     std::vector<int32_t> ag_run;  // index in ag of every chunk's run

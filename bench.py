@@ -323,6 +323,7 @@ def run_tide(args, rank, world, local_rank):
         G.set_ce_lanes(args.ce_lanes or 8)
     G1.close()
     legs["all_gather_register"] = time_ag_variant(G, buf, stream, b_ag, max(3, args.steps), args, "register")
+    legs["reduce_scatter_slots"] = time_rs_slots(G, g, buf, S, stream, max(3, args.steps))
     for leg in legs.values():
         leg["frac_of_peak"] = leg["gbs"] / peak
 
@@ -488,6 +489,39 @@ def slot_reuse(G, g, buf, S, U, stream):
     return {"stage_ms": stage_ms, "stage_gbs": 2 * grad_bytes / (stage_ms * 1e-3) / 1e9,
             "rs_from_slots_ms": rs_ms, "rs_in_place_ms": inplace_ms,
             "grad_bytes_released_after_staging": grad_bytes, "slot_bytes": g.R * g.R * S * 2}
+
+
+def time_rs_slots(G, g: Group, buf, S: int, stream, iters: int, d: int = 0) -> dict:
+    """The reduce-scatter's summing step as destination d would run it on R GPUs: its R staging
+    slots (filled here once, outside the timed launches, by device copies that stand in for the
+    exchange) summed into d's fp32 shard.  Bytes: the valid slot elements read (R x 2 B each) + S x 4
+    B written."""
+    from all_gather_tide_gb300 import exchange
+
+    slots = torch.empty(g.R, S, dtype=torch.bfloat16, device=buf.shards.device)
+    out = torch.empty(S, dtype=torch.float32, device=buf.shards.device)
+    valid = 0
+    for c in exchange.reduce_scatter_pulls(g.R, g.rows, g.row_len, d):
+        slots[c.src_rank, c.dst_off:c.dst_off + c.elems].copy_(
+            buf.grads[c.src_rank][c.param].view(-1)[c.src_off:c.src_off + c.elems])
+        valid += c.elems
+    nbytes = valid * 2 + S * 4
+    slot_list = list(slots)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            G.reduce_scatter_slots(d, slot_list, out, stream)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(iters)]
+        for e in ev:
+            e[0].record(stream)
+            G.reduce_scatter_slots(d, slot_list, out, stream)
+            e[1].record(stream)
+    torch.cuda.synchronize()
+    ms = [e[0].elapsed_time(e[1]) for e in ev]
+    avg = statistics.mean(ms)
+    del slots, out, slot_list
+    return {"gbs": nbytes / (avg * 1e-3) / 1e9, "ms": avg, "ms_median": statistics.median(ms), "bytes": nbytes,
+            "destination": d, "ctas": G.get_ctas()[0], "kernel": "reduce_scatter_bulk_kernel",
+            "what": "tide_reduce_scatter_slots: one destination's R staging slots summed into its fp32 shard"}
 
 
 def time_ag_variant(G, buf, stream, b_ag, iters, args, variant):

@@ -152,6 +152,28 @@ int tide_reduce_scatter(tide_group_t g, const void *const *grads, void *const *s
                         void *stream);
 
 /*
+ * tide_reduce_scatter_slots — the summing step of the same reduce-scatter when the R ranks are R
+ * GPUs (Fig. 2b: GPU d pulls slice d of every contributor, then step 5 sums; Fig. 6a: the sums are
+ * formed where the shard lives).  Destination rank d first receives, from every contributor r, the
+ * valid elements of its slice of each parameter into a staging slot (one contiguous copy per
+ * (r, p): elements [d*s_p, d*s_p + v(d,p)*L_p) of g_r,p to slot_r[o_p ..)); this call then sums the
+ * R slots into d's fp32 shard:
+ *     shard[o_p + i] = slot_0[o_p + i] + slot_1[o_p + i] + ... + slot_{R-1}[o_p + i],  i < v(d,p)*L_p
+ *     shard[o_p + i] = +0.0f                                                    v(d,p)*L_p <= i < s_p
+ * with the same widening, order and rounding as tide_reduce_scatter, so the shard has the bits of
+ * tide_reduce_scatter's shard d over the gradients the slots were filled from.
+ *   d:     destination rank, 0 <= d < R.
+ *   slots: host array of R device pointers, entry r = the bf16 slot (S elements) holding
+ *          contributor r's slice; padding positions of the slots are never read.
+ *   shard: device pointer to d's fp32 shard of S elements (overwritten).
+ * Runs the bulk-copy kernel with the group's reduce-scatter CTA count; slot pointers that are not
+ * 16-byte aligned take its element-wise path with the same results (or TIDE_EALIGN under
+ * TIDE_FLAG_VEC_STRICT).  Asynchronous on `stream`.  Errors: TIDE_EINVAL (null or misaligned
+ * pointers, d out of range, another device current), TIDE_ECUDA.
+ */
+int tide_reduce_scatter_slots(tide_group_t g, int32_t d, const void *const *slots, void *shard, void *stream);
+
+/*
  * tide_all_gather — all-gather placement, SM kernel (abstract: the all-gather lands each shard
  * in the parameters' own storage, with no copy-out; Fig. 1; Fig. 5b).  For every rank r and parameter p:
  *     param_p[r*s_p + i] = shard_r[o_p + i]      for i < v(r,p)*L_p

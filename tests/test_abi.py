@@ -104,6 +104,7 @@ def test_null_group_calls(tide):
     k = ctypes.c_int32()
     assert L.tide_group_ag_kernel(None, ctypes.byref(k)) == tide.TIDE_EINVAL
     assert L.tide_group_set_ce_bands(None, 2) == tide.TIDE_EINVAL
+    assert L.tide_reduce_scatter_slots(None, 0, arr, 16, None) == tide.TIDE_EINVAL
     assert L.tide_group_destroy(None) == tide.TIDE_OK
 
 

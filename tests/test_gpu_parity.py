@@ -712,3 +712,118 @@ def test_shards_need_only_fp32_alignment(tide):
             for d in range(g.R):
                 assert np.array_equal(f32_bits(shards[d]), want[d].view(np.uint32)), (off, variant, d)
             G.close()
+
+
+# ---- the summing step over staging slots (the reduce-scatter's local step on R GPUs) -----------
+
+
+def fill_slots(g, lay, grads, d, slots):
+    """Destination d's exchange, with device copies standing in for the copies from the other
+    GPUs: from every contributor r, its slice d of every parameter into slot r at o_p."""
+    from all_gather_tide_gb300 import exchange
+
+    for c in exchange.reduce_scatter_pulls(g.R, g.rows, g.row_len, d):
+        slots[c.src_rank][c.dst_off:c.dst_off + c.elems].copy_(grads[c.src_rank][c.param][c.src_off:c.src_off + c.elems])
+
+
+def run_rs_slots(tide, g, dests=None, ctas=0, misalign=False, flags=0):
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    host = rng.group_grads(g)
+    want = oracle.reduce_scatter(lay, [[t.numpy().view(np.uint16) for t in row] for row in host])
+    grads = [[t.cuda().view(-1) for t in row] for row in host]
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
+    G.set_ctas(ctas, 0)
+    off = 1 if misalign else 0
+    for d in (range(g.R) if dests is None else dests):
+        packed = Guarded(g.R * lay.S, torch.int16, fill=BF16_JUNK, offset_elems=off)  # junk in the padding
+        slots = [packed.view[r * lay.S:(r + 1) * lay.S] for r in range(g.R)]
+        fill_slots(g, lay, grads, d, slots)
+        shard = Guarded(lay.S, torch.float32, fill=F32_SENTINEL)
+        G.reduce_scatter_slots(d, slots, shard.view)
+        torch.cuda.synchronize()
+        assert G.device_status() == 0
+        got = f32_bits(shard.view)
+        bad = np.nonzero(got != want[d].view(np.uint32))[0]
+        assert bad.size == 0, f"{g.name}: shard {d} from slots differs at {bad[:8]} (of {bad.size})"
+        assert shard.guards_intact() and packed.guards_intact(), f"{g.name}: guard band overwritten ({d})"
+    G.close()
+
+
+def _slot_dests(g):
+    return None if g.R <= 16 else sorted({0, 1, g.R // 2, g.R - 1})
+
+
+@pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
+def test_reduce_scatter_slots_matches_oracle(tide, g):
+    run_rs_slots(tide, g, _slot_dests(g))
+
+
+@pytest.mark.parametrize("g", [group("tiny"), group("llama70b").scaled(32), edge_groups()[2], edge_groups()[3]],
+                         ids=lambda g: g.name)
+def test_reduce_scatter_slots_misaligned_slots(tide, g):
+    """Slots that are only 2-byte aligned take the element-wise path: same bits."""
+    run_rs_slots(tide, g, _slot_dests(g), misalign=True)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 16, 1000])
+def test_reduce_scatter_slots_cta_counts(tide, ctas):
+    run_rs_slots(tide, group("qwen3moe").scaled(16), [0, 5, 7], ctas=ctas)
+
+
+def test_reduce_scatter_slots_rejects_bad_arguments(tide):
+    g = group("tiny")
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_VEC_STRICT)
+    slots = torch.zeros(g.R, lay.S + 8, dtype=torch.int16, device="cuda")
+    shard = torch.zeros(lay.S + 1, dtype=torch.float32, device="cuda")
+    good = [slots[r, :lay.S] for r in range(g.R)]
+    for d in (-1, g.R):
+        with pytest.raises(tide.TideError) as e:
+            G.reduce_scatter_slots(d, good, shard)
+        assert e.value.status == tide.TIDE_EINVAL
+    odd = torch.zeros(lay.S + 1, dtype=torch.float32, device="cuda").view(torch.int16)[1:]  # 2-byte aligned only
+    with pytest.raises(tide.TideError) as e:
+        G.reduce_scatter_slots(0, good, odd)  # an fp32 shard needs 4-byte alignment
+    assert e.value.status == tide.TIDE_EINVAL
+    with pytest.raises(tide.TideError) as e:
+        G.reduce_scatter_slots(0, [slots[r, 1:lay.S + 1] for r in range(g.R)], shard)
+    assert e.value.status == tide.TIDE_EALIGN  # VEC_STRICT: slots not 16-byte aligned
+    G.close()
+
+
+@pytest.mark.parametrize("name", ["llama70b", "wan_r64"])
+def test_full_size_reduce_scatter_slots(tide, name):
+    """Full-size groups at the default grid, first and last destination: sampled outputs computed
+    one by one by the oracle, and every piece equal to torch fp32 adds in ascending rank order."""
+    g = group(name)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    grads = [[rng.grad_bits(g, r, p, device="cuda").view(-1) for p in range(g.P)] for r in range(g.R)]
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
+    slots = torch.empty(g.R, lay.S, dtype=torch.int16, device="cuda")
+    shard = torch.empty(lay.S, dtype=torch.float32, device="cuda")
+    dd_all, jj_all = _sample_positions(lay, seed=7 + len(name))
+    for d in (0, g.R - 1):
+        slots.fill_(BF16_JUNK)
+        shard.view(torch.int32).fill_(F32_SENTINEL)
+        fill_slots(g, lay, grads, d, list(slots))
+        G.reduce_scatter_slots(d, list(slots), shard)
+        torch.cuda.synchronize()
+        assert G.device_status() == 0
+        j = jj_all[dd_all == d]
+        want = oracle.rs_points(lay, np.full(j.shape, d, np.int64), j,
+                                lambda r, p, idx: rng.grad_bits(g, r, p, idx=torch.from_numpy(idx)).numpy().view(np.uint16))
+        got = shard[torch.from_numpy(j).cuda()]
+        assert np.array_equal(f32_bits(got), want.view(np.uint32)), d
+        for p in range(g.P):
+            o, s, L = int(lay.o[p]), int(lay.s[p]), int(lay.row_len[p])
+            v = lay.valid_rows(d, p) * L
+            piece = shard[o:o + s]
+            assert bool((piece[v:].view(torch.int32) == 0).all()), (d, p)
+            if v:
+                acc = grads[0][p][d * s: d * s + v].view(torch.bfloat16).float()
+                for r in range(1, g.R):
+                    acc = acc + grads[r][p][d * s: d * s + v].view(torch.bfloat16).float()
+                assert torch.equal(piece[:v].view(torch.int32), acc.view(torch.int32)), (d, p)
+    G.close()
+    del grads, slots, shard
+    torch.cuda.empty_cache()
