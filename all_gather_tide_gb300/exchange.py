@@ -7,8 +7,8 @@ all-gather landing in parameter storage):
 
 * reduce-scatter: GPU d pulls, from every contributor r, the slice of each parameter it will own,
   elements [d*s_p, d*s_p + v(d,p)*L_p) of g_r,p, into staging slot r at the slice's shard offset
-  o_p; it then sums its R staging slots (its own slot read in place) in ascending rank order into
-  its fp32 shard, so the result is the single-GPU result bit for bit;
+  o_p; it then sums its R staging slots in ascending rank order into its fp32 shard
+  (``tide_reduce_scatter_slots``), so the result is the single-GPU result bit for bit;
 * all-gather: GPU d pulls, from every source rank r, the valid rows of each parameter piece,
   elements [o_p, o_p + v(r,p)*L_p) of shard_r, straight to element r*s_p of its parameter p.
 

@@ -2,9 +2,10 @@
 and 3): every rank pulls exactly its slices, in the planned order, and the results match the
 oracle's single-process reduce-scatter and all-gather bit for bit.
 
-The local summing step, which on GPUs would be a kernel over the staging slots, is stood in for by
-torch fp32 adds in ascending rank order; what is tested here is the plan: which rank sends which
-elements to whom, the offsets on both sides and the order of the exchange.
+The local summing step, which on GPUs is the library's kernel over the staging slots
+(tide_reduce_scatter_slots, checked against the oracle on a GPU in test_gpu_parity.py), is stood in
+for here by torch fp32 adds in ascending rank order; what is tested here is the plan: which rank
+sends which elements to whom, the offsets on both sides and the order of the exchange.
 """
 import os
 import socket
