@@ -323,7 +323,9 @@ def run_tide(args, rank, world, local_rank):
         G.set_ce_lanes(args.ce_lanes or 8)
     G1.close()
     legs["all_gather_register"] = time_ag_variant(G, buf, stream, b_ag, max(3, args.steps), args, "register")
-    legs["reduce_scatter_slots"] = time_rs_slots(G, g, buf, S, stream, max(3, args.steps))
+    # the summing step always runs the bulk-copy kernel: the caller's count, else one CTA per SM
+    slot_ctas = args.rs_ctas or torch.cuda.get_device_properties(dev).multi_processor_count
+    legs["reduce_scatter_slots"] = time_rs_slots(G, g, buf, S, stream, max(3, args.steps), slot_ctas)
     for leg in legs.values():
         leg["frac_of_peak"] = leg["gbs"] / peak
 
@@ -491,7 +493,7 @@ def slot_reuse(G, g, buf, S, U, stream):
             "grad_bytes_released_after_staging": grad_bytes, "slot_bytes": g.R * g.R * S * 2}
 
 
-def time_rs_slots(G, g: Group, buf, S: int, stream, iters: int, d: int = 0) -> dict:
+def time_rs_slots(G, g: Group, buf, S: int, stream, iters: int, ctas: int, d: int = 0) -> dict:
     """The reduce-scatter's summing step as destination d would run it on R GPUs: its R staging
     slots (filled here once, outside the timed launches, by device copies that stand in for the
     exchange) summed into d's fp32 shard.  Bytes: the valid slot elements read (R x 2 B each) + S x 4
@@ -520,7 +522,7 @@ def time_rs_slots(G, g: Group, buf, S: int, stream, iters: int, d: int = 0) -> d
     avg = statistics.mean(ms)
     del slots, out, slot_list
     return {"gbs": nbytes / (avg * 1e-3) / 1e9, "ms": avg, "ms_median": statistics.median(ms), "bytes": nbytes,
-            "destination": d, "ctas": G.get_ctas()[0], "kernel": "reduce_scatter_bulk_kernel",
+            "destination": d, "ctas": ctas, "kernel": "reduce_scatter_bulk_kernel",
             "what": "tide_reduce_scatter_slots: one destination's R staging slots summed into its fp32 shard"}
 
 
