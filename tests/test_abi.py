@@ -3,6 +3,8 @@ planner matches the oracle's on every workload, and argument checks fail before 
 import ctypes
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -148,3 +150,19 @@ def test_header_constants_match_binding(tide):
             assert getattr(tide, name) == v, name
             seen += 1
     assert seen >= 15
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without libtide.so the binding raises on first use: there is no fallback path."""
+    code = (
+        "import all_gather_tide_gb300 as t\n"
+        f"t.LIB_PATH = {str(tmp_path / 'libtide.so')!r}\n"
+        "t._lib = None\n"
+        "try:\n"
+        "    t.Group(2, [(4, 3)])\n"
+        "except RuntimeError as e:\n"
+        "    assert 'missing' in str(e), e\n"
+        "    print('raised')\n"
+    )
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, cwd=ROOT, timeout=300)
+    assert out.returncode == 0 and out.stdout.strip() == "raised", out.stdout + out.stderr
