@@ -58,6 +58,7 @@ SIGNATURES = {
     "tide_group_get_ctas": (ctypes.c_int, [_vp, _i32p, _i32p]),
     "tide_reduce_scatter": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_reduce_scatter_slots": (ctypes.c_int, [_vp, ctypes.c_int32, _vpp, _vp, _vp]),
+    "tide_stage_slices": (ctypes.c_int, [_vp, ctypes.c_int32, _vpp, _vpp, _vp]),
     "tide_all_gather": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_all_gather_ce": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_group_last_ce_copies": (ctypes.c_int, [_vp, _i64p, _i32p]),
@@ -231,6 +232,13 @@ def tide_reduce_scatter(g: int, grads, shards: Sequence, stream=None) -> None:
            "tide_reduce_scatter")
 
 
+def tide_stage_slices(g: int, d: int, grads, slots: Sequence, stream=None) -> None:
+    """Copies slice d of every contributor's gradients into ``slots`` (R bf16 tensors of S elements)
+    at the shard offsets, one copy-engine copy per (contributor, parameter)."""
+    _check(lib().tide_stage_slices(g, d, _ptr_array(_flat_grads(grads)), _ptr_array(slots), _stream(stream)),
+           "tide_stage_slices")
+
+
 def tide_reduce_scatter_slots(g: int, d: int, slots: Sequence, shard, stream=None) -> None:
     """``slots``: R bf16 staging slots of S elements (slot r holds contributor r's slice d of every
     parameter at o_p); ``shard``: d's fp32 shard of S elements."""
@@ -377,6 +385,9 @@ class Group:
 
     def reduce_scatter(self, grads, shards, stream=None) -> None:
         tide_reduce_scatter(self.handle, grads, shards, stream)
+
+    def stage_slices(self, d: int, grads, slots, stream=None) -> None:
+        tide_stage_slices(self.handle, d, grads, slots, stream)
 
     def reduce_scatter_slots(self, d: int, slots, shard, stream=None) -> None:
         tide_reduce_scatter_slots(self.handle, d, slots, shard, stream)

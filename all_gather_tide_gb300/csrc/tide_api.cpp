@@ -717,6 +717,38 @@ int tide_stage_into_slots(tide_group_t g, const void* const* grads, void* const*
     return lanes.end();
 }
 
+int tide_stage_slices(tide_group_t g, int32_t d, const void* const* grads, void* const* slots, void* stream) {
+    if (!g || !grads || !slots) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    const tide::Plan& pl = g->plan;
+    const int R = pl.R, P = pl.P;
+    if (d < 0 || d >= R) return TIDE_EINVAL;
+    for (size_t i = 0; i < size_t(R) * P; ++i)
+        if (!grads[i] || !elem_aligned(grads[i], 2)) return TIDE_EINVAL;
+    for (int r = 0; r < R; ++r)
+        if (!slots[r] || !elem_aligned(slots[r], 2)) return TIDE_EINVAL;
+    int rc = check_device(g);
+    if (rc != TIDE_OK) return rc;
+    CeLanes lanes{g, static_cast<cudaStream_t>(stream)};
+    if ((rc = lanes.begin()) != TIDE_OK) return rc;
+    // contributors d+1, ..., R-1, 0, ..., d; within one, parameters in order
+    for (int k = 1; k <= R; ++k) {
+        const int r = (d + k) % R;
+        for (int p = 0; p < P; ++p) {
+            const int64_t n = tide::valid_rows(pl.rows[p], pl.m[p], d) * pl.row_len[p];
+            if (n == 0) continue;
+            const char* src = static_cast<const char*>(grads[size_t(r) * P + p]) + int64_t(d) * pl.s[p] * 2;
+            char* dst = static_cast<char*>(slots[r]) + pl.o[p] * 2;
+            cudaError_t e = cudaMemcpyAsync(dst, src, size_t(n) * 2, cudaMemcpyDeviceToDevice, lanes.pick(n * 2));
+            if (e != cudaSuccess) {
+                lanes.end();  // join the helper lanes back before reporting
+                return cuda_fail(e);
+            }
+        }
+    }
+    return lanes.end();
+}
+
 int tide_group_last_ce_copies(tide_group_t g, int64_t* copies, int32_t* uniform_pitch) {
     if (!g || !copies || !uniform_pitch) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);

@@ -494,10 +494,12 @@ def slot_reuse(G, g, buf, S, U, stream):
 
 
 def time_rs_slots(G, g: Group, buf, S: int, stream, iters: int, ctas: int, d: int = 0) -> dict:
-    """The reduce-scatter's summing step as destination d would run it on R GPUs: its R staging
-    slots (filled here once, outside the timed launches, by device copies that stand in for the
-    exchange) summed into d's fp32 shard.  Bytes: the valid slot elements read (R x 2 B each) + S x 4
-    B written."""
+    """The reduce-scatter as destination d would run it on R GPUs: the exchange that fills its R
+    staging slots (tide_stage_slices: copy-engine copies, here device to device) and the summing
+    step (tide_reduce_scatter_slots) into d's fp32 shard, each timed on its own.  Bytes of the sum:
+    the valid slot elements read (2 B each) + S x 4 B written; of the exchange: the same elements
+    read and written (2 + 2 B each)."""
+    import all_gather_tide_gb300 as tide
     from all_gather_tide_gb300 import exchange
 
     slots = torch.empty(g.R, S, dtype=torch.bfloat16, device=buf.shards.device)
@@ -509,6 +511,18 @@ def time_rs_slots(G, g: Group, buf, S: int, stream, iters: int, ctas: int, d: in
         valid += c.elems
     nbytes = valid * 2 + S * 4
     slot_list = list(slots)
+    # the exchange, through the library (it rewrites the same elements the copies above wrote)
+    grads = tide.pointer_table([t for row in buf.grads for t in row])
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            G.stage_slices(d, grads, slot_list, stream)
+        sev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(iters)]
+        for e in sev:
+            e[0].record(stream)
+            G.stage_slices(d, grads, slot_list, stream)
+            e[1].record(stream)
+    torch.cuda.synchronize()
+    sms = statistics.mean([e[0].elapsed_time(e[1]) for e in sev])
     with torch.cuda.stream(stream):
         for _ in range(2):
             G.reduce_scatter_slots(d, slot_list, out, stream)
@@ -523,7 +537,10 @@ def time_rs_slots(G, g: Group, buf, S: int, stream, iters: int, ctas: int, d: in
     del slots, out, slot_list
     return {"gbs": nbytes / (avg * 1e-3) / 1e9, "ms": avg, "ms_median": statistics.median(ms), "bytes": nbytes,
             "destination": d, "ctas": ctas, "kernel": "reduce_scatter_bulk_kernel",
-            "what": "tide_reduce_scatter_slots: one destination's R staging slots summed into its fp32 shard"}
+            "what": "tide_reduce_scatter_slots: one destination's R staging slots summed into its fp32 shard",
+            "exchange": {"gbs": valid * 4 / (sms * 1e-3) / 1e9, "ms": sms, "bytes": valid * 4,
+                         "what": "tide_stage_slices: the R*P copies that fill the slots, copy engines over the "
+                                 "group's lanes, device to device on one GPU"}}
 
 
 def time_ag_variant(G, buf, stream, b_ag, iters, args, variant):

@@ -174,6 +174,20 @@ int tide_reduce_scatter(tide_group_t g, const void *const *grads, void *const *s
 int tide_reduce_scatter_slots(tide_group_t g, int32_t d, const void *const *slots, void *shard, void *stream);
 
 /*
+ * tide_stage_slices — the exchange that fills destination d's staging slots for
+ * tide_reduce_scatter_slots (Fig. 2b: GPU d pulls slice d of every contributor).  For every
+ * contributor r, in the order d+1, ..., R-1, 0, ..., d, and every parameter p with v(d,p) > 0, one
+ * cudaMemcpyAsync (copy engines; spread over the group's copy-engine lanes, stream-ordered with
+ * `stream` on both sides) of elements [d*s_p, d*s_p + v(d,p)*L_p) of grads[r*P + p] to element o_p
+ * of slots[r].  Padding positions of the slots are not written.
+ *   grads: host array of R*P device pointers, as in tide_reduce_scatter.
+ *   slots: host array of R device pointers, bf16 slots of S elements each.
+ * Errors: TIDE_EINVAL (null or misaligned pointers, d out of range, another device current),
+ * TIDE_ECUDA.
+ */
+int tide_stage_slices(tide_group_t g, int32_t d, const void *const *grads, void *const *slots, void *stream);
+
+/*
  * tide_all_gather — all-gather placement, SM kernel (abstract: the all-gather lands each shard
  * in the parameters' own storage, with no copy-out; Fig. 1; Fig. 5b).  For every rank r and parameter p:
  *     param_p[r*s_p + i] = shard_r[o_p + i]      for i < v(r,p)*L_p

@@ -726,18 +726,23 @@ def fill_slots(g, lay, grads, d, slots):
         slots[c.src_rank][c.dst_off:c.dst_off + c.elems].copy_(grads[c.src_rank][c.param][c.src_off:c.src_off + c.elems])
 
 
-def run_rs_slots(tide, g, dests=None, ctas=0, misalign=False, flags=0):
+def run_rs_slots(tide, g, dests=None, ctas=0, misalign=False, flags=0, library_staging=False, lanes=0):
     lay = oracle.plan(g.R, g.rows, g.row_len)
     host = rng.group_grads(g)
     want = oracle.reduce_scatter(lay, [[t.numpy().view(np.uint16) for t in row] for row in host])
     grads = [[t.cuda().view(-1) for t in row] for row in host]
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
     G.set_ctas(ctas, 0)
+    if lanes:
+        G.set_ce_lanes(lanes)
     off = 1 if misalign else 0
     for d in (range(g.R) if dests is None else dests):
         packed = Guarded(g.R * lay.S, torch.int16, fill=BF16_JUNK, offset_elems=off)  # junk in the padding
         slots = [packed.view[r * lay.S:(r + 1) * lay.S] for r in range(g.R)]
-        fill_slots(g, lay, grads, d, slots)
+        if library_staging:
+            G.stage_slices(d, grads, slots)  # copy engines, on the same stream as the sum
+        else:
+            fill_slots(g, lay, grads, d, slots)
         shard = Guarded(lay.S, torch.float32, fill=F32_SENTINEL)
         G.reduce_scatter_slots(d, slots, shard.view)
         torch.cuda.synchronize()
@@ -763,6 +768,18 @@ def test_reduce_scatter_slots_matches_oracle(tide, g):
 def test_reduce_scatter_slots_misaligned_slots(tide, g):
     """Slots that are only 2-byte aligned take the element-wise path: same bits."""
     run_rs_slots(tide, g, _slot_dests(g), misalign=True)
+
+
+@pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
+def test_stage_slices_then_sum_matches_oracle(tide, g):
+    """The library's own exchange copies (tide_stage_slices) followed by the summing step."""
+    run_rs_slots(tide, g, _slot_dests(g), library_staging=True)
+
+
+@pytest.mark.parametrize("lanes", [1, 3, 8])
+def test_stage_slices_lanes_stay_stream_ordered(tide, lanes):
+    run_rs_slots(tide, group("qwen3moe").scaled(16), [0, 3, 7], library_staging=True, lanes=lanes)
+    run_rs_slots(tide, edge_groups()[2], None, library_staging=True, lanes=lanes, misalign=True)
 
 
 @pytest.mark.parametrize("ctas", [1, 3, 16, 1000])
