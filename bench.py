@@ -453,7 +453,13 @@ def stock_comparator(G, g, buf, S, U, stream, legs):
                            "sm_time": sm_time, "max_abs_diff_vs_direct": err},
         "all_gather_copy_out": {"ms": ag_ms, "gbs_of_direct_bytes": b_ag / (ag_ms * 1e-3) / 1e9,
                                 "direct_ms": legs["all_gather_sm"]["ms"], "speedup_direct": ag_ms / legs["all_gather_sm"]["ms"],
-                                "op": "torch.split_with_sizes_copy into padded [R, m_p*L_p] storage"},
+                                "op": "torch.split_with_sizes_copy into padded [R, m_p*L_p] storage",
+                                # Table 6's SM-ms column: the copy-out fills the GPU, the SM placement
+                                # holds its CTAs (at most one per SM), the copy-engine placement no SM
+                                "sm_time": {"stock_copy_out_sm_ms": ag_ms * sms,
+                                            "direct_sm_sm_ms": legs["all_gather_sm"]["ms"]
+                                            * min(legs["all_gather_sm"]["ctas"], sms),
+                                            "direct_ce_sm_ms": 0.0}},
     }
     del sp, out_shards
     torch.cuda.empty_cache()
