@@ -1004,95 +1004,113 @@ def end_to_end(G, g, buf, S, U, dev, args, world):
     """Same step through the public API with host buffers: every step copies all its inputs in
     from pinned host memory and all its outputs back, inside the timed region.  Input copies are
     spread over several streams (several copy engines), and step k+1's input copies overlap step
-    k's output copies (opposite directions of the host link); events keep every buffer's reuse
-    ordered after its last reader."""
+    k's output copies (opposite directions of the host link).  The steps alternate between two sets
+    of device buffers, so step k+1's input copies also overlap step k's kernels; events keep every
+    buffer's reuse ordered after its last reader.  The same loop over one device set is reported
+    beside it."""
     h_grads = [[t.to("cpu").pin_memory() for t in row] for row in buf.grads]
     h_ag = buf.ag_in.to("cpu").pin_memory()
     h_shards = torch.empty(g.R, S, dtype=torch.float32).pin_memory()
     h_params = [torch.empty(g.numel(p), dtype=torch.bfloat16).pin_memory() for p in range(g.P)]
     h2d = sum(t.numel() * 2 for row in h_grads for t in row) + h_ag.numel() * 2
     d2h = h_shards.numel() * 4 + sum(t.numel() * 2 for t in h_params)
+    sets = [buf, Buffers(g, S, dev)]  # the second set's contents are overwritten by the copies
     n_in = 4
     s_in = [torch.cuda.Stream(device=dev) for _ in range(n_in)]
     s_c = torch.cuda.Stream(device=dev)
     s_out = torch.cuda.Stream(device=dev)
-    pairs_in = [(buf.grads[r][p], h_grads[r][p]) for r in range(g.R) for p in range(g.P)] + [(buf.ag_in, h_ag)]
-    pairs_in.sort(key=lambda x: -x[0].numel())
-    lanes = [[] for _ in range(n_in)]
-    load = [0] * n_in
-    for d_t, h_t in pairs_in:  # balance the bytes over the input streams
-        k = load.index(min(load))
-        lanes[k].append((d_t, h_t))
-        load[k] += d_t.numel()
-    pairs_out = [(h_shards, buf.shards)] + [(h_params[p], buf.params[p]) for p in range(g.P)]
-    state = {"computed": None, "copied_out": None}
 
-    def step():
-        for k in range(n_in):
-            if state["computed"] is not None:
-                s_in[k].wait_event(state["computed"])  # the previous step's kernels have read the inputs
-            with torch.cuda.stream(s_in[k]):
-                for d_t, h_t in lanes[k]:
+    def plan_lanes(b):
+        pairs = [(b.grads[r][p], h_grads[r][p]) for r in range(g.R) for p in range(g.P)] + [(b.ag_in, h_ag)]
+        pairs.sort(key=lambda x: -x[0].numel())
+        lanes, load = [[] for _ in range(n_in)], [0] * n_in
+        for d_t, h_t in pairs:  # balance the bytes over the input streams
+            k = load.index(min(load))
+            lanes[k].append((d_t, h_t))
+            load[k] += d_t.numel()
+        return lanes
+
+    lanes = [plan_lanes(b) for b in sets]
+    outs = [[(h_shards, b.shards)] + [(h_params[p], b.params[p]) for p in range(g.P)] for b in sets]
+    state = {"k": 0, "computed": [None, None], "copied_out": [None, None]}
+
+    def step(nsets):
+        k = state["k"] % nsets
+        state["k"] += 1
+        b = sets[k]
+        for i in range(n_in):
+            if state["computed"][k] is not None:
+                s_in[i].wait_event(state["computed"][k])  # the set's last kernels have read its inputs
+            with torch.cuda.stream(s_in[i]):
+                for d_t, h_t in lanes[k][i]:
                     d_t.copy_(h_t, non_blocking=True)
-        for k in range(n_in):
-            s_c.wait_stream(s_in[k])
-        if state["copied_out"] is not None:
-            s_c.wait_event(state["copied_out"])  # the previous step's outputs have been copied out
-        G.reduce_scatter(buf.grads, buf.shard_list, s_c)
-        G.all_gather(buf.ag_list, buf.params, s_c)
+        for i in range(n_in):
+            s_c.wait_stream(s_in[i])
+        if state["copied_out"][k] is not None:
+            s_c.wait_event(state["copied_out"][k])  # the set's last outputs have been copied out
+        G.reduce_scatter(b.grads, b.shard_list, s_c)
+        G.all_gather(b.ag_list, b.params, s_c)
         computed = torch.cuda.Event()
         computed.record(s_c)
         s_out.wait_event(computed)
         with torch.cuda.stream(s_out):
-            for h_t, d_t in pairs_out:
+            for h_t, d_t in outs[k]:
                 h_t.copy_(d_t, non_blocking=True)
         copied_out = torch.cuda.Event()
         copied_out.record(s_out)
-        state["computed"], state["copied_out"] = computed, copied_out
+        state["computed"][k], state["copied_out"][k] = computed, copied_out
 
     def one_direction(direction):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
         e0.record(s_c)
-        for k in range(n_in):
-            s_in[k].wait_event(e0)
-            with torch.cuda.stream(s_in[k]):
-                for d_t, h_t in lanes[k]:
+        for i in range(n_in):
+            s_in[i].wait_event(e0)
+            with torch.cuda.stream(s_in[i]):
+                for d_t, h_t in lanes[0][i]:
                     if direction == "h2d":
                         d_t.copy_(h_t, non_blocking=True)
                     else:
                         h_t.copy_(d_t, non_blocking=True)
-        for k in range(n_in):
-            s_c.wait_stream(s_in[k])
+        for i in range(n_in):
+            s_c.wait_stream(s_in[i])
         e1.record(s_c)
         torch.cuda.synchronize()
         return h2d / (e0.elapsed_time(e1) * 1e-3) / 1e9
 
     steps = max(2, min(args.steps, args.e2e_steps))
     h2d_before = one_direction("h2d")  # the host link varies with the machine's other tenants
-    for _ in range(2):
-        step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    # five timed windows of `steps` steps; the median window is reported (the host link is shared
-    # with the machine's other tenants, and single windows varied by up to 1.8x)
-    windows = []
-    for _ in range(5):
-        state["computed"] = state["copied_out"] = None
+
+    def windows_of(nsets, n=5):
+        for _ in range(2):
+            step(nsets)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s_c)
-        for k in range(n_in):
-            s_in[k].wait_event(e0)
-        for _ in range(steps):
-            step()
-        s_c.wait_stream(s_out)
-        e1.record(s_c)
-        torch.cuda.synchronize()
-        windows.append(max_over_ranks(e0.elapsed_time(e1), world, dev))
+        if world > 1:
+            torch.distributed.barrier()
+        # n timed windows of `steps` steps; the median window is reported (the host link is shared
+        # with the machine's other tenants, and single windows varied by up to 1.8x)
+        out = []
+        for _ in range(n):
+            state["computed"], state["copied_out"], state["k"] = [None, None], [None, None], 0
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s_c)
+            for i in range(n_in):
+                s_in[i].wait_event(e0)
+            for _ in range(steps):
+                step(nsets)
+            s_c.wait_stream(s_out)
+            e1.record(s_c)
+            torch.cuda.synchronize()
+            out.append(max_over_ranks(e0.elapsed_time(e1), world, dev))
+        return out
+
+    windows = windows_of(2)
     ms = sorted(windows)[len(windows) // 2]
-    value = whole_job_gbs(rs_bytes(g, S, U) + ag_bytes(U), steps, world, ms)
+    windows1 = windows_of(1, 3)
+    ms1 = sorted(windows1)[len(windows1) // 2]
+    step_bytes = rs_bytes(g, S, U) + ag_bytes(U)
+    value = whole_job_gbs(step_bytes, steps, world, ms)
     link = {"h2d_gbs_inputs_only_before": h2d_before, "h2d_gbs_inputs_only": one_direction("h2d"),
             "d2h_gbs_same_bytes": one_direction("d2h")}
     # a step cannot be shorter than its input copies over the host link alone, at the fastest rate
@@ -1100,15 +1118,19 @@ def end_to_end(G, g, buf, S, U, dev, args, world):
     h2d_ms = h2d / (max(h2d_before, link["h2d_gbs_inputs_only"]) * 1e9) * 1e3
     link["h2d_bound_ms_per_step"] = h2d_ms
     link["frac_of_h2d_bound"] = h2d_ms / (ms / steps)
-    del h_grads, h_ag, h_shards, h_params, pairs_in, pairs_out, lanes
+    del h_grads, h_ag, h_shards, h_params, lanes, outs, sets
     if hasattr(torch._C, "_host_emptyCache"):  # hand the 20 GB of pinned buffers back to the host
         torch._C._host_emptyCache()
+    torch.cuda.empty_cache()
     return {"value": value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "steps": steps, "ms_per_step": ms / steps, "host_link": link,
-            "windows_gbs": [whole_job_gbs(rs_bytes(g, S, U) + ag_bytes(U), steps, world, w) for w in windows],
+            "windows_gbs": [whole_job_gbs(step_bytes, steps, world, w) for w in windows],
+            "one_device_set": {"value": whole_job_gbs(step_bytes, steps, world, ms1), "ms_per_step": ms1 / steps,
+                               "windows_gbs": [whole_job_gbs(step_bytes, steps, world, w) for w in windows1]},
             "how": "pinned host -> device copies of all inputs (4 streams), tide_reduce_scatter + "
-                   "tide_all_gather, device -> pinned host copies of all outputs, every step; step k+1's "
-                   "input copies overlap step k's output copies; median of 5 windows"}
+                   "tide_all_gather, device -> pinned host copies of all outputs, every step; two device "
+                   "buffer sets in turn, so step k+1's input copies overlap step k's kernels and output "
+                   "copies; median of 5 windows"}
 
 
 # ---- the host oracle ---------------------------------------------------------------------------
