@@ -29,6 +29,18 @@ int cuda_fail(cudaError_t e) {
         if (e_ != cudaSuccess) return cuda_fail(e_);      \
     } while (0)
 
+// A copy enqueued on one of the copy-engine lanes: on failure the helper lanes are joined back to
+// the caller's stream (so nothing already enqueued on them outlives the call unordered) before the
+// error is reported.
+#define TIDE_LANE_COPY(lanes, call)                       \
+    do {                                                  \
+        cudaError_t e_ = (call);                          \
+        if (e_ != cudaSuccess) {                          \
+            (lanes).end();                                \
+            return cuda_fail(e_);                         \
+        }                                                 \
+    } while (0)
+
 // One entry of the ring of pointer tables.  The host copy is pinned so the upload is a true
 // asynchronous copy on the caller's stream; `done` is recorded after the kernel that reads the
 // device copy, so the slot is only rewritten once that kernel has finished.
@@ -595,17 +607,17 @@ int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* p
             const int64_t nb = std::min<int64_t>(g->ce_bands, f);
             for (int64_t b = 0; b < nb; ++b) {
                 const int64_t r0 = f * b / nb, r1 = f * (b + 1) / nb;
-                TIDE_CUDA(cudaMemcpy2DAsync(dst + r0 * piece_bytes, size_t(piece_bytes),
-                                            base + r0 * pitch + pl.o[p] * 2, size_t(pitch), size_t(piece_bytes),
-                                            size_t(r1 - r0), cudaMemcpyDeviceToDevice,
-                                            lanes.pick((r1 - r0) * piece_bytes)));
+                TIDE_LANE_COPY(lanes, cudaMemcpy2DAsync(dst + r0 * piece_bytes, size_t(piece_bytes),
+                                                        base + r0 * pitch + pl.o[p] * 2, size_t(pitch),
+                                                        size_t(piece_bytes), size_t(r1 - r0), cudaMemcpyDeviceToDevice,
+                                                        lanes.pick((r1 - r0) * piece_bytes)));
                 ++copies;
             }
             const int64_t rest = pl.rows[p] - f * pl.m[p];
             if (rest > 0) {
                 const int64_t bytes = rest * pl.row_len[p] * 2;
-                TIDE_CUDA(cudaMemcpyAsync(dst + f * piece_bytes, base + f * pitch + pl.o[p] * 2, size_t(bytes),
-                                          cudaMemcpyDeviceToDevice, lanes.pick(bytes)));
+                TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst + f * piece_bytes, base + f * pitch + pl.o[p] * 2,
+                                                      size_t(bytes), cudaMemcpyDeviceToDevice, lanes.pick(bytes)));
                 ++copies;
             }
         } else {
@@ -613,8 +625,9 @@ int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* p
                 const int64_t v = tide::valid_rows(pl.rows[p], pl.m[p], r);
                 if (v == 0) continue;
                 const int64_t bytes = v * pl.row_len[p] * 2;
-                TIDE_CUDA(cudaMemcpyAsync(dst + r * piece_bytes, static_cast<const char*>(shards[r]) + pl.o[p] * 2,
-                                          size_t(bytes), cudaMemcpyDeviceToDevice, lanes.pick(bytes)));
+                TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst + r * piece_bytes,
+                                                      static_cast<const char*>(shards[r]) + pl.o[p] * 2, size_t(bytes),
+                                                      cudaMemcpyDeviceToDevice, lanes.pick(bytes)));
                 ++copies;
             }
         }
@@ -708,8 +721,8 @@ int tide_stage_into_slots(tide_group_t g, const void* const* grads, void* const*
         const int64_t n = pl.rows[p] * pl.row_len[p];
         for (int r = 0; r < R; ++r) {
             char* dst = static_cast<char*>(slots[r]) + off * 2;
-            TIDE_CUDA(cudaMemcpyAsync(dst, grads[size_t(r) * P + p], size_t(n) * 2, cudaMemcpyDeviceToDevice,
-                                      lanes.pick(n * 2)));
+            TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst, grads[size_t(r) * P + p], size_t(n) * 2,
+                                                  cudaMemcpyDeviceToDevice, lanes.pick(n * 2)));
             staged[size_t(r) * P + p] = dst;
         }
         off += n;
@@ -739,11 +752,7 @@ int tide_stage_slices(tide_group_t g, int32_t d, const void* const* grads, void*
             if (n == 0) continue;
             const char* src = static_cast<const char*>(grads[size_t(r) * P + p]) + int64_t(d) * pl.s[p] * 2;
             char* dst = static_cast<char*>(slots[r]) + pl.o[p] * 2;
-            cudaError_t e = cudaMemcpyAsync(dst, src, size_t(n) * 2, cudaMemcpyDeviceToDevice, lanes.pick(n * 2));
-            if (e != cudaSuccess) {
-                lanes.end();  // join the helper lanes back before reporting
-                return cuda_fail(e);
-            }
+            TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst, src, size_t(n) * 2, cudaMemcpyDeviceToDevice, lanes.pick(n * 2)));
         }
     }
     return lanes.end();
