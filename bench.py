@@ -1117,7 +1117,11 @@ def end_to_end(G, g, buf, S, U, dev, args, world):
     # the link gave in this run
     h2d_ms = h2d / (max(h2d_before, link["h2d_gbs_inputs_only"]) * 1e9) * 1e3
     link["h2d_bound_ms_per_step"] = h2d_ms
-    link["frac_of_h2d_bound"] = h2d_ms / (ms / steps)
+    frac = h2d_ms / (ms / steps)
+    # above 1 the link ran faster during the windows than when it was measured: no bound then
+    link["frac_of_h2d_bound"] = frac if frac <= 1.0 else None
+    if frac > 1.0:
+        link["note"] = "the link measured slower than the windows ran: its rate changed during the run"
     del h_grads, h_ag, h_shards, h_params, lanes, outs, sets
     if hasattr(torch._C, "_host_emptyCache"):  # hand the 20 GB of pinned buffers back to the host
         torch._C._host_emptyCache()
