@@ -26,7 +26,7 @@
  *     inputs must stay alive and unmodified, and their outputs untouched, until the stream has
  *     executed the call.  Errors raised by the kernels themselves surface at the next
  *     synchronisation of that stream; argument errors are returned before anything is enqueued.
- *   - Host pointer arrays (grads, shards, params) are copied before the call returns.
+ *   - Host pointer arrays (grads, shards, params, slots) are copied before the call returns.
  *   - The caller owns every device buffer.  A group owns only its plan tables (device), a small
  *     ring of pinned host / device pointer tables and CUDA events; tide_group_destroy frees them.
  *   - A group may be used from several host threads; calls on one group are serialised.
@@ -46,7 +46,8 @@ extern "C" {
 #define TIDE_EINVAL (-1)  /* null pointer, R < 1, P < 1, rows < 1, row_len < 1, bad index, wrong device,
                             or a device pointer not aligned to its element (2 bytes bf16, 4 bytes fp32) */
 #define TIDE_EALIGN (-2)  /* TIDE_FLAG_VEC_STRICT set and a pointer that needs 16-byte alignment lacks it
-                            (reduce-scatter: a gradient; placement: a shard or a parameter) */
+                            (reduce-scatter: a gradient or a staging slot; placement: a shard or a
+                            parameter) */
 #define TIDE_ELAYOUT (-3) /* TIDE_FLAG_CE_STRICT set and the shards are not at a uniform pitch */
 #define TIDE_ECUDA (-4)   /* a CUDA runtime call failed; tide_last_cuda_error() gives its code */
 #define TIDE_ENOMEM (-5)  /* host or device allocation of the group's own tables failed */
@@ -58,7 +59,7 @@ extern "C" {
 /* ---- group flags ------------------------------------------------------------------------- */
 /* Return TIDE_EALIGN instead of running the element-wise path when a pointer whose 16-byte
  * alignment the vector paths need is not 16-byte aligned: a gradient for tide_reduce_scatter, a
- * shard or a parameter for tide_all_gather. */
+ * staging slot for tide_reduce_scatter_slots, a shard or a parameter for tide_all_gather. */
 #define TIDE_FLAG_VEC_STRICT 0x1u
 /* With TIDE_FLAG_CE_2D: return TIDE_ELAYOUT from tide_all_gather_ce instead of falling back to
  * 1-D copies when shards[r] != shards[0] + r*pitch for one pitch >= S*2 bytes. */
