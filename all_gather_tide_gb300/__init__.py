@@ -58,6 +58,8 @@ SIGNATURES = {
     "tide_group_get_ctas": (ctypes.c_int, [_vp, _i32p, _i32p]),
     "tide_reduce_scatter": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_reduce_scatter_slots": (ctypes.c_int, [_vp, ctypes.c_int32, _vpp, _vp, _vp]),
+    "tide_probe_mixed": (ctypes.c_int, [_vp, ctypes.c_int64, _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]),
     "tide_stage_slices": (ctypes.c_int, [_vp, ctypes.c_int32, _vpp, _vpp, _vp]),
     "tide_all_gather": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_all_gather_ce": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
@@ -337,6 +339,16 @@ def tide_probe_ingest(buf, bulk_bytes: int, ldg_bytes: int, ctas: int, copy_byte
     ``out`` is a device uint32/int32 tensor of 2 entries."""
     _check(lib().tide_probe_ingest(_ptr(buf), bulk_bytes, ldg_bytes, ctas, copy_bytes, stages, consumer_warps,
                                    ldg_warps, _ptr(out), _stream(stream)), "tide_probe_ingest")
+
+
+def tide_probe_mixed(buf, bulk_bytes: int, st_buf, st_bytes: int, ctas: int, copy_bytes: int, stages: int,
+                     consumer_warps: int, st_warps: int, out, stream=None) -> None:
+    """Per-SM read/write sharing probe (bulk copies read out of shared memory while other warps
+    write 32-byte vectors); ``out`` is a device int64 tensor of 3 entries (checksum, error flags,
+    bytes written)."""
+    _check(lib().tide_probe_mixed(_ptr(buf), bulk_bytes, _ptr(st_buf) if st_buf is not None else None, st_bytes,
+                                  ctas, copy_bytes, stages, consumer_warps, st_warps, _ptr(out), _stream(stream)),
+           "tide_probe_mixed")
 
 
 # ---- convenience object -----------------------------------------------------------------------

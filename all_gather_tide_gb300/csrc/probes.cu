@@ -266,6 +266,142 @@ ingest_kernel(const unsigned char* __restrict__ buf, int64_t bulk_bytes, const u
     if (x) atomicXor(&out[0], x);
 }
 
+
+// Reads [buf, buf + bulk_bytes) like ingest_kernel's bulk part (warp 0 lane 0 issues `copy_bytes`
+// copies through `stages` slots, `consumers` warps read every 16-byte word of a landed slot) while
+// `st_warps` warps write 32-byte vectors into this CTA's share of [st, st + st_bytes), cycling over
+// it, until the reads are done (or, with bulk_bytes == 0, for one pass).  out[0] ^= checksum of the
+// reads, out[1] |= error flags (1: a wait expired, 2: copies still landing, 4: the writers hit their
+// 2 s bound), out[2] += bytes written.  Every loop is bounded by the buffer or by %globaltimer.
+__global__ void __launch_bounds__(512, 1)
+mixed_kernel(const unsigned char* __restrict__ buf, int64_t bulk_bytes, unsigned char* __restrict__ st,
+             int64_t st_bytes, int copy_bytes, int stages, int consumers, int st_warps, unsigned long long* out) {
+    extern __shared__ __align__(128) unsigned char sm[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(sm);
+    uint64_t* empty = full + 16;
+    unsigned char* data = sm + 256;
+    __shared__ int abort_flag;
+    __shared__ int reads_done;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&full[s])));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(&empty[s])), "r"(consumers));
+        }
+        abort_flag = 0;
+        reads_done = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    volatile int* abort = &abort_flag;
+    volatile int* done = &reads_done;
+    const uint64_t limit = 1000000000ull;
+    auto try_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        return ok != 0;
+    };
+    auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+        const uint64_t t0 = now_ns();
+        uint32_t n = 0;
+        while (!try_wait(bar, parity)) {
+            if ((++n & 255) == 0) {
+                if (*abort) return false;
+                if (now_ns() - t0 > limit) {
+                    *abort = 1;
+                    atomicOr(&out[1], 1ull);
+                    return false;
+                }
+            }
+        }
+        return true;
+    };
+    const int64_t nchunk = bulk_bytes / copy_bytes;
+    if (warp == 0) {
+        if (lane == 0) {
+            int64_t k = 0;
+            for (int64_t c = blockIdx.x; c < nchunk; c += gridDim.x, ++k) {
+                const int s = int(k % stages);
+                if (!wait(&empty[s], uint32_t(((k / stages) & 1) ^ 1))) break;
+                asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&full[s])),
+                             "r"(copy_bytes)
+                             : "memory");
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                        smem_u32(data + int64_t(s) * copy_bytes)),
+                    "l"(buf + c * copy_bytes), "r"(copy_bytes), "r"(smem_u32(&full[s]))
+                    : "memory");
+            }
+            // every issued copy lands before the CTA exits (bounded); then the writers may stop
+            const uint64_t t0 = now_ns();
+            for (int64_t j = k > stages ? k - stages : 0; j < k; ++j) {
+                while (!try_wait(&full[j % stages], uint32_t((j / stages) & 1))) {
+                    if (now_ns() - t0 > limit) {
+                        atomicOr(&out[1], 2ull);
+                        break;
+                    }
+                }
+            }
+            *done = 1;
+        }
+        return;
+    }
+    if (warp <= consumers) {
+        const int ctid = (warp - 1) * 32 + lane;
+        const int words = copy_bytes / 16;
+        uint32_t x = 0;
+        int64_t k = 0;
+        for (int64_t c = blockIdx.x; c < nchunk; c += gridDim.x, ++k) {
+            const int s = int(k % stages);
+            if (!wait(&full[s], uint32_t((k / stages) & 1))) break;
+            const uint4* row = reinterpret_cast<const uint4*>(data + int64_t(s) * copy_bytes);
+            for (int i = ctid; i < words; i += consumers * 32) {
+                const uint4 w = row[i];
+                x ^= w.x ^ w.y ^ w.z ^ w.w;
+            }
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[s])) : "memory");
+        }
+        if (x) atomicXor(&out[0], (unsigned long long)x);
+        return;
+    }
+    if (warp <= consumers + st_warps) {
+        // this CTA's share of the write region, in 32-byte vectors
+        const int64_t nvec = st_bytes / 32;
+        const int64_t per = nvec / gridDim.x;
+        const int64_t v0 = int64_t(blockIdx.x) * per;
+        const int t = (warp - consumers - 1) * 32 + lane, nt = st_warps * 32;
+        const uint32_t val = 0x9e3779b9u * uint32_t(blockIdx.x * 1024 + t);
+        const uint64_t t0 = now_ns();
+        const bool one_pass = bulk_bytes == 0;
+        int64_t written = 0, it = 0;
+        bool stop = per <= 0;
+        while (!stop) {
+            for (int64_t v = t; v < per; v += nt) {
+                float* p = reinterpret_cast<float*>(st + (v0 + v) * 32);
+                const float f = __uint_as_float(val ^ uint32_t(v));
+                asm volatile("st.global.cs.v8.f32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1};" ::"l"(p), "f"(f) : "memory");
+                written += 32;
+                if (!one_pass && (++it & 63) == 0 && *done) {
+                    stop = true;
+                    break;
+                }
+            }
+            if (one_pass || *done) break;
+            if (now_ns() - t0 > 2 * limit) {
+                atomicOr(&out[1], 4ull);
+                break;
+            }
+        }
+        atomicAdd(&out[2], (unsigned long long)written);
+    }
+}
+
 }  // namespace
 }  // namespace tide
 
@@ -325,6 +461,25 @@ int tide_probe_ingest(const void* buf, int64_t bulk_bytes, int64_t ldg_bytes, in
     tide::ingest_kernel<<<ctas, 32 * (1 + consumers + ldg_warps), smem, static_cast<cudaStream_t>(stream)>>>(
         base, bulk_bytes, base + ldg_off, ldg_bytes, copy_bytes, stages, consumers, consumer_warps > 0 ? 1 : 0,
         ldg_warps, out);
+    e = cudaGetLastError();
+    return e == cudaSuccess ? TIDE_OK : tide::record_cuda_error(e);
+}
+
+int tide_probe_mixed(const void* buf, int64_t bulk_bytes, void* st_buf, int64_t st_bytes, int32_t ctas,
+                     int32_t copy_bytes, int32_t stages, int32_t consumer_warps, int32_t st_warps, uint64_t* out,
+                     void* stream) {
+    if (!buf || !out || (st_warps > 0 && !st_buf) || bulk_bytes < 0 || st_bytes < 0 || ctas < 1 ||
+        copy_bytes < 16 || copy_bytes % 16 || stages < 1 || stages > 16 ||
+        256 + int64_t(copy_bytes) * stages > int64_t(tide::kMaxDynamicSmem) || consumer_warps < 1 || st_warps < 0 ||
+        1 + consumer_warps + st_warps > 16 || (reinterpret_cast<uintptr_t>(buf) & 255u) ||
+        (reinterpret_cast<uintptr_t>(st_buf) & 31u) || st_bytes % 32)
+        return TIDE_EINVAL;
+    const int smem = 256 + copy_bytes * stages;
+    cudaError_t e = cudaFuncSetAttribute(tide::mixed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return tide::record_cuda_error(e);
+    tide::mixed_kernel<<<ctas, 32 * (1 + consumer_warps + st_warps), smem, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const unsigned char*>(buf), bulk_bytes, static_cast<unsigned char*>(st_buf), st_bytes, copy_bytes,
+        stages, consumer_warps, st_warps, reinterpret_cast<unsigned long long*>(out));
     e = cudaGetLastError();
     return e == cudaSuccess ? TIDE_OK : tide::record_cuda_error(e);
 }

@@ -689,7 +689,19 @@ def interference(G, buf, stream, dev, args):
     read_bytes = 2 * G.R * G.U
     bound = 16 * ing["ceiling_gbs_per_sm"] * b_rs / read_bytes
     out["sm_ingest_16_ctas"] = ing
+    mixed = sm_mixed(dev, stream, ctas=16)
+    out["sm_mixed_16_ctas"] = mixed
     if "operating_point" in out:
+        # the tighter bound: reads and writes share an SM's traffic, and the reduce-scatter writes
+        # R*S*4 bytes for every R*U*2 it reads
+        per_sm, rd = mixed_bound(mixed["rows"], (b_rs - read_bytes) / read_bytes)
+        if per_sm is not None:
+            out["operating_point"]["bound_16_sms_mixed_gbs"] = 16 * per_sm
+            out["operating_point"]["bound_16_sms_mixed_frac"] = 16 * per_sm / peak
+            out["operating_point"]["rs_alone_over_mixed_bound"] = out["operating_point"]["rs_gbs_alone"] / (16 * per_sm)
+            out["operating_point"]["bound_mixed_rule"] = (
+                "16 x the bytes one SM moves at the reduce-scatter's ratio of bytes written to bytes read, "
+                "interpolated between tide_probe_mixed's measured (read, write) points")
         out["operating_point"]["bound_16_sms_gbs"] = bound
         out["operating_point"]["bound_16_sms_frac"] = bound / peak
         out["operating_point"]["bound_rule"] = ("16 x the most bytes per second any ingest-probe mode brought into "
@@ -775,6 +787,66 @@ def sm_ingest(dev, stream, full=False, ctas=16):
     torch.cuda.empty_cache()
     best = max(rows, key=lambda r: r["gbs_per_sm"])
     return {"ctas": ctas, "rows": rows, "ceiling_gbs_per_sm": best["gbs_per_sm"], "ceiling_mode": best["mode"]}
+
+
+def sm_mixed(dev, stream, ctas=16):
+    """How reads and writes share one SM (tide_probe_mixed, `ctas` CTAs, one per SM): 32-byte
+    stores alone, bulk copies read out of shared memory alone, and both at once with 1 to 7 of the
+    CTA's 16 warps writing.  A reduce-scatter over R = 8 ranks writes 4 bytes per 16 read."""
+    import all_gather_tide_gb300 as tide
+
+    nb, ns = 2 << 30, 1 << 30
+    buf = torch.empty(nb // 4, dtype=torch.int32, device=dev)
+    buf.fill_(0x3C00_3C00)
+    st = torch.empty(ns, dtype=torch.uint8, device=dev)
+    out = torch.zeros(3, dtype=torch.int64, device=dev)
+    cases = [("writes only", 73728, 3, 1, 14, False), ("writes only", 73728, 3, 1, 4, False),
+             ("reads only", 73728, 3, 15, 0, True), ("reads and writes", 73728, 3, 14, 1, True),
+             ("reads and writes", 73728, 3, 13, 2, True), ("reads and writes", 73728, 3, 12, 3, True),
+             ("reads and writes", 73728, 3, 11, 4, True),
+             ("reads and writes", 73728, 3, 8, 7, True), ("reads only", 46080, 5, 15, 0, True),
+             ("reads and writes", 46080, 5, 14, 1, True)]
+
+    def launch(copy, stages, cons, stw, reads):
+        bulk = nb // copy * copy if reads else 0
+        tide.tide_probe_mixed(buf, bulk, st, ns, ctas, copy, stages, cons, stw, out, stream)
+        return bulk
+
+    with torch.cuda.stream(stream):
+        for _ in range(10):  # bring the clocks up
+            launch(73728, 3, 15, 0, True)
+    torch.cuda.synchronize()
+    rows = []
+    for name, copy, stages, cons, stw, reads in cases:
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            launch(copy, stages, cons, stw, reads)
+            out[2].zero_()
+            ev[0].record(stream)
+            n = sum(launch(copy, stages, cons, stw, reads) for _ in range(3))
+            ev[1].record(stream)
+        torch.cuda.synchronize()
+        s = ev[0].elapsed_time(ev[1]) * 1e-3
+        w = int(out[2].item())
+        rows.append({"mode": name, "copy_bytes": copy, "stages": stages, "consumer_warps": cons, "st_warps": stw,
+                     "read_gbs_per_sm": n / s / 1e9 / ctas, "write_gbs_per_sm": w / s / 1e9 / ctas})
+    assert int(out[1].item()) == 0, "a probe wait expired"
+    del buf, st
+    torch.cuda.empty_cache()
+    return {"ctas": ctas, "rows": rows}
+
+
+def mixed_bound(rows, write_per_read: float):
+    """Bytes per second (read + written) one SM can move at a given ratio of bytes written to bytes
+    read, interpolated between the probe's measured points of the 72 KB x 3 geometry (reads alone,
+    then 1, 2, 3, 4 and 7 writer warps), linear in the ratio; None outside the measured range."""
+    pts = sorted((r["write_gbs_per_sm"] / r["read_gbs_per_sm"], r["read_gbs_per_sm"]) for r in rows
+                 if r["copy_bytes"] == 73728 and r["read_gbs_per_sm"] > 0)
+    for (x0, r0), (x1, r1) in zip(pts, pts[1:]):
+        if x0 <= write_per_read <= x1:
+            rd = r0 + (r1 - r0) * (write_per_read - x0) / (x1 - x0) if x1 > x0 else min(r0, r1)
+            return rd * (1.0 + write_per_read), rd
+    return None, None
 
 
 def cta_sweep(G, buf, stream, args, concurrent):

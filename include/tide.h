@@ -386,6 +386,24 @@ int tide_probe_bulk_read(const void *buf, int64_t bytes, int32_t ctas, int32_t c
 int tide_probe_ingest(const void *buf, int64_t bulk_bytes, int64_t ldg_bytes, int32_t ctas, int32_t copy_bytes,
                       int32_t stages, int32_t consumer_warps, int32_t ldg_warps, uint32_t *out, void *stream);
 
+/*
+ * tide_probe_mixed — how reading and writing share one SM's traffic, the other half of the bound of
+ * a reduce-scatter that may hold only a few SMs (it writes one fp32 sum per R bf16 values read).
+ * `ctas` CTAs (one per SM: each claims copy_bytes*stages of shared memory) read [buf, buf +
+ * bulk_bytes) as tide_probe_ingest's bulk part does (`consumer_warps` >= 1 warps read every 16-byte
+ * word of each landed copy; buf 256-byte aligned) while `st_warps` warps per CTA write 32-byte
+ * vectors into the CTA's equal share of [st_buf, st_buf + st_bytes) (st_buf 32-byte aligned,
+ * st_bytes a multiple of 32), cycling over it until that CTA's reads have landed; with bulk_bytes
+ * == 0 they write their share once.  The written values are a pattern of no meaning; nothing else
+ * is written.  1 + consumer_warps + st_warps <= 16.
+ * out (device, 3 uint64): out[0] ^= checksum of what was read, out[1] |= 1 if a wait (1 s bound)
+ * expired, 2 if copies were still landing 1 s after the last issue, 4 if the writers stopped at
+ * their 2 s bound; out[2] += bytes written.  TIDE_EINVAL on bad arguments.
+ */
+int tide_probe_mixed(const void *buf, int64_t bulk_bytes, void *st_buf, int64_t st_bytes, int32_t ctas,
+                     int32_t copy_bytes, int32_t stages, int32_t consumer_warps, int32_t st_warps, uint64_t *out,
+                     void *stream);
+
 /* ---- errors ------------------------------------------------------------------------------ */
 const char *tide_strerror(int status);
 /* cudaError_t code of the last CUDA failure reported as TIDE_ECUDA on this host thread. */

@@ -97,3 +97,18 @@ def test_host_oracle_parts_give_the_whole_group_result():
     params = oracle.all_gather(ho.lay, ho.shards, [np.zeros(g.numel(p), np.uint16) for p in range(g.P)])
     for p in range(g.P):
         assert np.array_equal(ho.params[p], params[p])
+
+
+def test_mixed_bound_interpolates_between_probe_points():
+    import bench
+
+    rows = [{"copy_bytes": 73728, "read_gbs_per_sm": r, "write_gbs_per_sm": w}
+            for r, w in [(150.0, 0.0), (120.0, 24.0), (50.0, 50.0)]]
+    rows.append({"copy_bytes": 46080, "read_gbs_per_sm": 300.0, "write_gbs_per_sm": 0.0})  # other geometry: ignored
+    per_sm, rd = bench.mixed_bound(rows, 0.0)
+    assert (per_sm, rd) == (150.0, 150.0)
+    per_sm, rd = bench.mixed_bound(rows, 0.2)  # exactly the second point
+    assert abs(rd - 120.0) < 1e-9 and abs(per_sm - 144.0) < 1e-9
+    per_sm, rd = bench.mixed_bound(rows, 0.6)  # halfway from ratio 0.2 to 1.0: reads halfway from 120 to 50
+    assert abs(rd - 85.0) < 1e-9 and abs(per_sm - 85.0 * 1.6) < 1e-9
+    assert bench.mixed_bound(rows, 1.5) == (None, None)

@@ -69,3 +69,43 @@ def test_ingest_probe_reads_every_byte(tide, consumers, ldg_warps):
     got = out.cpu().numpy().view(np.uint32)
     assert got[1] == 0
     assert got[0] == want
+
+
+def test_mixed_probe_writes_its_pattern_once(tide):
+    """Writers alone (no reads): every 32-byte vector of each CTA's share holds the pattern of the
+    thread that wrote it, the bytes beyond the shares are untouched, and the count is exact."""
+    ctas, st_warps = 16, 4
+    nt = st_warps * 32
+    st_bytes = (64 << 20) + 96  # shares of whole vectors; 96 bytes left over
+    per = st_bytes // 32 // ctas
+    st = torch.full((st_bytes // 4 + 64,), -1, dtype=torch.int32, device="cuda")
+    src = torch.zeros(1024, dtype=torch.int32, device="cuda")
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    tide.tide_probe_mixed(src, 0, st, st_bytes, ctas, 73728, 3, 1, st_warps, out)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    assert o[1] == 0 and o[2] == per * 32 * ctas
+    w = st.cpu().numpy().view(np.uint32)
+    vec = w[: ctas * per * 8].reshape(ctas, per, 8)
+    b = np.arange(ctas, dtype=np.uint64)[:, None]
+    v = np.arange(per, dtype=np.uint64)[None, :]
+    want = ((np.uint64(0x9E3779B9) * (b * np.uint64(1024) + v % np.uint64(nt))) % np.uint64(1 << 32)).astype(np.uint32)
+    want ^= v.astype(np.uint32)
+    assert np.array_equal(vec, np.repeat(want[:, :, None], 8, axis=2))
+    assert np.all(w[ctas * per * 8:] == 0xFFFFFFFF)
+
+
+@pytest.mark.parametrize("consumers,st_warps", [(15, 0), (11, 4), (14, 1)])
+def test_mixed_probe_reads_every_byte_while_writing(tide, consumers, st_warps):
+    copy, stages = 73728, 3
+    bulk = (96 << 20) // copy * copy
+    buf = torch.randint(-2**31, 2**31 - 1, (bulk // 4 + 64,), dtype=torch.int32, device="cuda")
+    st = torch.empty(32 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    tide.tide_probe_mixed(buf, bulk, st, st.numel(), 16, copy, stages, consumers, st_warps, out)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    want = np.bitwise_xor.reduce(buf.cpu().numpy().view(np.uint32)[: bulk // 4])
+    assert o[1] == 0
+    assert np.uint32(o[0] & 0xFFFFFFFF) == want
+    assert (o[2] > 0) == (st_warps > 0)
