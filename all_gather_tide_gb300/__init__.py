@@ -34,6 +34,7 @@ TIDE_FLAG_CE_1D = 0x10
 TIDE_RS_AUTO = 0
 TIDE_RS_REGISTER = 1
 TIDE_RS_BULK = 2
+TIDE_RS_TMEM = 3
 TIDE_AG_AUTO = 0
 TIDE_AG_REGISTER = 1
 TIDE_AG_BULK = 2
@@ -59,7 +60,8 @@ SIGNATURES = {
     "tide_reduce_scatter": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_reduce_scatter_slots": (ctypes.c_int, [_vp, ctypes.c_int32, _vpp, _vp, _vp]),
     "tide_probe_mixed": (ctypes.c_int, [_vp, ctypes.c_int64, _vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
-                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp, _vp]),
+                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                        ctypes.c_int32, _vp, _vp]),
     "tide_stage_slices": (ctypes.c_int, [_vp, ctypes.c_int32, _vpp, _vpp, _vp]),
     "tide_all_gather": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
     "tide_all_gather_ce": (ctypes.c_int, [_vp, _vpp, _vpp, _vp]),
@@ -342,12 +344,14 @@ def tide_probe_ingest(buf, bulk_bytes: int, ldg_bytes: int, ctas: int, copy_byte
 
 
 def tide_probe_mixed(buf, bulk_bytes: int, st_buf, st_bytes: int, ctas: int, copy_bytes: int, stages: int,
-                     consumer_warps: int, st_warps: int, out, stream=None) -> None:
+                     consumer_warps: int, st_warps: int, out, stream=None, burst_rows: int = 0,
+                     burst_vecs: int = 0) -> None:
     """Per-SM read/write sharing probe (bulk copies read out of shared memory while other warps
     write 32-byte vectors); ``out`` is a device int64 tensor of 3 entries (checksum, error flags,
     bytes written)."""
     _check(lib().tide_probe_mixed(_ptr(buf), bulk_bytes, _ptr(st_buf) if st_buf is not None else None, st_bytes,
-                                  ctas, copy_bytes, stages, consumer_warps, st_warps, _ptr(out), _stream(stream)),
+                                  ctas, copy_bytes, stages, consumer_warps, st_warps, burst_rows, burst_vecs,
+                                  _ptr(out), _stream(stream)),
            "tide_probe_mixed")
 
 

@@ -275,7 +275,8 @@ ingest_kernel(const unsigned char* __restrict__ buf, int64_t bulk_bytes, const u
 // 2 s bound), out[2] += bytes written.  Every loop is bounded by the buffer or by %globaltimer.
 __global__ void __launch_bounds__(512, 1)
 mixed_kernel(const unsigned char* __restrict__ buf, int64_t bulk_bytes, unsigned char* __restrict__ st,
-             int64_t st_bytes, int copy_bytes, int stages, int consumers, int st_warps, unsigned long long* out) {
+             int64_t st_bytes, int copy_bytes, int stages, int consumers, int st_warps, int burst_rows, int burst_vecs,
+             unsigned long long* out) {
     extern __shared__ __align__(128) unsigned char sm[];
     uint64_t* full = reinterpret_cast<uint64_t*>(sm);
     uint64_t* empty = full + 16;
@@ -354,6 +355,12 @@ mixed_kernel(const unsigned char* __restrict__ buf, int64_t bulk_bytes, unsigned
     if (warp <= consumers) {
         const int ctid = (warp - 1) * 32 + lane;
         const int words = copy_bytes / 16;
+        // burst writes: after every `burst_rows` landed copies each reading thread stores
+        // `burst_vecs` 32-byte vectors (adjacent threads, adjacent vectors) into this CTA's share of
+        // the write region, as a reduce-scatter stores its sums after the last rank's row
+        const int64_t per = burst_rows > 0 ? st_bytes / 32 / gridDim.x : 0;
+        const int64_t v0 = int64_t(blockIdx.x) * per;
+        int64_t cursor = 0, written = 0;
         uint32_t x = 0;
         int64_t k = 0;
         for (int64_t c = blockIdx.x; c < nchunk; c += gridDim.x, ++k) {
@@ -366,8 +373,20 @@ mixed_kernel(const unsigned char* __restrict__ buf, int64_t bulk_bytes, unsigned
             }
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&empty[s])) : "memory");
+            if (per > 0 && (k + 1) % burst_rows == 0) {
+                const float f = __uint_as_float(x | 1u);
+                for (int b = 0; b < burst_vecs; ++b) {
+                    const int64_t v = (cursor + int64_t(b) * consumers * 32 + ctid) % per;
+                    float* p = reinterpret_cast<float*>(st + (v0 + v) * 32);
+                    asm volatile("st.global.cs.v8.f32 [%0], {%1, %1, %1, %1, %1, %1, %1, %1};" ::"l"(p), "f"(f)
+                                 : "memory");
+                }
+                cursor = (cursor + int64_t(burst_vecs) * consumers * 32) % per;
+                written += int64_t(burst_vecs) * 32;
+            }
         }
         if (x) atomicXor(&out[0], (unsigned long long)x);
+        if (written) atomicAdd(&out[2], (unsigned long long)written);
         return;
     }
     if (warp <= consumers + st_warps) {
@@ -466,8 +485,10 @@ int tide_probe_ingest(const void* buf, int64_t bulk_bytes, int64_t ldg_bytes, in
 }
 
 int tide_probe_mixed(const void* buf, int64_t bulk_bytes, void* st_buf, int64_t st_bytes, int32_t ctas,
-                     int32_t copy_bytes, int32_t stages, int32_t consumer_warps, int32_t st_warps, uint64_t* out,
-                     void* stream) {
+                     int32_t copy_bytes, int32_t stages, int32_t consumer_warps, int32_t st_warps, int32_t burst_rows,
+                     int32_t burst_vecs, uint64_t* out, void* stream) {
+    if (burst_rows < 0 || burst_vecs < 0 || (burst_rows > 0 && (!st_buf || st_bytes / 32 < ctas)))
+        return TIDE_EINVAL;
     if (!buf || !out || (st_warps > 0 && !st_buf) || bulk_bytes < 0 || st_bytes < 0 || ctas < 1 ||
         copy_bytes < 16 || copy_bytes % 16 || stages < 1 || stages > 16 ||
         256 + int64_t(copy_bytes) * stages > int64_t(tide::kMaxDynamicSmem) || consumer_warps < 1 || st_warps < 0 ||
@@ -479,7 +500,7 @@ int tide_probe_mixed(const void* buf, int64_t bulk_bytes, void* st_buf, int64_t 
     if (e != cudaSuccess) return tide::record_cuda_error(e);
     tide::mixed_kernel<<<ctas, 32 * (1 + consumer_warps + st_warps), smem, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const unsigned char*>(buf), bulk_bytes, static_cast<unsigned char*>(st_buf), st_bytes, copy_bytes,
-        stages, consumer_warps, st_warps, reinterpret_cast<unsigned long long*>(out));
+        stages, consumer_warps, st_warps, burst_rows, burst_vecs, reinterpret_cast<unsigned long long*>(out));
     e = cudaGetLastError();
     return e == cudaSuccess ? TIDE_OK : tide::record_cuda_error(e);
 }

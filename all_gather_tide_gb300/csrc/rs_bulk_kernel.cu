@@ -369,6 +369,262 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, const int32_t* __rest
     }
 }
 
+
+// The widest stores a destination address allows (bytes: 32, 16, 8 or 4; shards need only fp32
+// alignment) and 8 fp32 sums stored with them, evict-first.
+__device__ __forceinline__ int store_width(const float* p) {
+    const unsigned da = unsigned(reinterpret_cast<uintptr_t>(p) & 31u);
+    return da == 0 ? 32 : (da & 15u) == 0 ? 16 : (da & 7u) == 0 ? 8 : 4;
+}
+
+__device__ __forceinline__ void store8(float* p, const float (&a)[8], int sw) {
+    if (sw == 32) {
+        st_cs_v8(p, a);
+    } else if (sw == 16) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(a[0], a[1], a[2], a[3]));
+        __stcs(reinterpret_cast<float4*>(p + 4), make_float4(a[4], a[5], a[6], a[7]));
+    } else if (sw == 8) {
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) __stcs(reinterpret_cast<float2*>(p + k), make_float2(a[k], a[k + 1]));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) __stcs(p + k, a[k]);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// TMEM-staged variant: the same pipeline and the same sums, but the consumers never store to
+// global memory.  Measured on GB300 with the read/write probe (16 CTAs): stores issued by the warps
+// that read the landed copies cut their reads from ~110 to ~55-67 GB/s per SM, whether issued in
+// bursts or spread out, while the same stores from separate warps cost the reads ~5 %.  So here the
+// consumers hand each chunk's fp32 sums to Tensor Memory (tcgen05.st, the SM's 256 KB accumulator
+// memory, otherwise unused by this kernel; two chunk buffers) and one writer warp per SM
+// sub-partition drains them to the shard (tcgen05.ld, then 32-byte stores), and also writes the
+// elements the bulk copies do not carry (tails, padding, element-wise pieces).  A warp reaches only
+// the TMEM lanes of its own sub-partition (lanes 32 * (warp % 4) ...), so consumer warp w parks
+// its sums in lane quarter w % 4 and the writer of that quarter drains them.
+//
+// Warps 0..14: consumers (6 groups of 8 sums per thread, as in reduce_scatter_bulk_kernel);
+// warp 15: producer; warps 16..19: writers of lane quarters 0..3.  640 threads, one CTA per SM.
+constexpr int kTmemWriters = 4;
+constexpr int kTmemThreads = (kBulkConsumerWarps + 1 + kTmemWriters) * 32;
+constexpr int kTmemGroups = int(kBulkChunk / 8 / (kBulkConsumerWarps * 32));  // 6
+constexpr uint32_t kTmemCols = 512;                                             // whole TMEM
+constexpr uint32_t kTmemBufCols = 4 * kTmemGroups * 8;                          // 4 consumers per quarter
+static_assert(2 * kTmemBufCols <= kTmemCols, "two chunk buffers must fit in TMEM");
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float (&a)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(__float_as_uint(a[0])), "r"(__float_as_uint(a[1])), "r"(__float_as_uint(a[2])),
+                 "r"(__float_as_uint(a[3])), "r"(__float_as_uint(a[4])), "r"(__float_as_uint(a[5])),
+                 "r"(__float_as_uint(a[6])), "r"(__float_as_uint(a[7]))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&a)[8]) {
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
+#pragma unroll
+    for (int k = 0; k < 8; ++k) a[k] = __uint_as_float(r[k]);
+}
+
+__global__ void __launch_bounds__(kTmemThreads, 1)
+reduce_scatter_tmem_kernel(const RsSeg* __restrict__ segs, const int32_t* __restrict__ chunk_piece, int64_t nchunks,
+                           const uint16_t* const* __restrict__ grads, float* const* __restrict__ shards, int R,
+                           int P, int allow_vec, int stages, int* status, uint64_t timeout_ns, int inject) {
+    constexpr int kConsumers = kBulkConsumerWarps * 32;
+    constexpr int kGroups = kTmemGroups;
+    static_assert(kBulkChunk == int64_t(kGroups) * 8 * kConsumers, "chunk must split evenly over the consumers");
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kBulkMaxStages;
+    unsigned char* data = smem + 128;
+    const uint16_t** gptr = reinterpret_cast<const uint16_t**>(data + int64_t(stages) * kBulkChunk * 2);
+    __shared__ int abort_flag;
+    __shared__ uint32_t tmem_base;
+    __shared__ __align__(8) uint64_t tfull[2];   // a chunk buffer holds the consumers' sums (15 arrivals)
+    __shared__ __align__(8) uint64_t tempty[2];  // a chunk buffer has been drained (4 arrivals)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int kProducer = kBulkConsumerWarps;
+    constexpr int kWriter0 = kBulkConsumerWarps + 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kBulkConsumerWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], kBulkConsumerWarps);
+            mbar_init(&tempty[b], kTmemWriters);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kWriter0) {  // one warp allocates the whole TMEM of this SM (one CTA per SM)
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tbase = tmem_base;
+    volatile int* abort = &abort_flag;
+
+    if (warp == kProducer) {
+        // ---------------- producer: as in reduce_scatter_bulk_kernel ----------------
+        PieceCursor pc;
+        int64_t it = 0;
+        int s = 0;
+        uint32_t phase = 0;
+        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+            if (pc.seek(segs, chunk_piece, c)) {
+                for (int r = lane; r < R; r += 32) gptr[r] = grads[int64_t(r) * P + pc.p];
+                __syncwarp();
+            }
+            const ChunkView v = pc.view(c, kBulkChunk, allow_vec);
+            if (v.nbulk == 0) continue;
+            int stop = 0;
+            if (lane == 0) {
+                const uint32_t bytes = uint32_t(v.nbulk * 2);
+                for (int r = 0; r < R; ++r) {
+                    if (!wait_bounded(&empty[s], phase ^ 1u, timeout_ns, abort, status, 2)) {
+                        stop = 1;
+                        break;
+                    }
+                    if (!inject) {
+                        mbar_arrive_expect_tx(&full[s], bytes);
+                        bulk_g2s(data + int64_t(s) * kBulkChunk * 2, gptr[r] + v.src, bytes, &full[s]);
+                    }
+                    ++it;
+                    if (++s == stages) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (__shfl_sync(0xffffffffu, stop, 0)) break;
+        }
+        if (lane == 0 && !inject) {
+            const uint64_t drain = globaltimer() + 100000000ull;
+            for (int64_t j = max(int64_t(0), it - stages); j < it; ++j) {
+                uint64_t* bar = &full[j % stages];
+                const uint32_t par = uint32_t((j / stages) & 1);
+                bool late = false;
+                while (!mbar_try_wait(bar, par)) {
+                    if (globaltimer() > drain) {
+                        atomicCAS(status, 0, 4);
+                        late = true;
+                        break;
+                    }
+                }
+                if (late) break;
+            }
+        }
+    } else if (warp < kProducer) {
+        // ---------------- consumers: sums in registers, handed to TMEM per chunk ----------------
+        const int ctid = threadIdx.x;
+        // this warp's 48 columns in lane quarter warp % 4 (the 32 lanes of its threads)
+        const uint32_t tq = tbase + (uint32_t(32 * (warp & 3)) << 16) + uint32_t((warp >> 2) * kGroups * 8);
+        PieceCursor pc;
+        int s = 0;
+        uint32_t phase = 0;
+        int64_t nb = 0;  // bulk chunks handed over so far
+        bool ok = true;
+        for (int64_t c = blockIdx.x; c < nchunks && ok; c += gridDim.x) {
+            pc.seek(segs, chunk_piece, c);
+            const ChunkView v = pc.view(c, kBulkChunk, allow_vec);
+            if (v.nbulk == 0) continue;
+            const bool whole = v.nbulk == kBulkChunk;
+            float acc[kGroups][8];
+            for (int r = 0; r < R; ++r) {
+                // every lane waits; the warp goes on only if all of them saw the stage land, so the
+                // warp-wide instructions below always run converged
+                if (!__all_sync(0xffffffffu, wait_bounded(&full[s], phase, timeout_ns, abort, status, 1))) {
+                    ok = false;
+                    break;
+                }
+                const uint4* row = reinterpret_cast<const uint4*>(data + int64_t(s) * kBulkChunk * 2);
+                uint4 w[kGroups];
+                load_row<kGroups, kConsumers>(w, row, ctid, whole, v.nbulk);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+                if (r == 0) add_row<true, kGroups>(acc, w);
+                else add_row<false, kGroups>(acc, w);
+                if (++s == stages) {
+                    s = 0;
+                    phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            // the chunk buffer must have been drained by all four writers (its use two chunks ago)
+            const int b = int(nb & 1);
+            if (!__all_sync(0xffffffffu,
+                            wait_bounded(&tempty[b], uint32_t(((nb >> 1) & 1) ^ 1), timeout_ns, abort, status, 16)))
+                break;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t tb = tq + uint32_t(b) * kTmemBufCols;
+#pragma unroll
+            for (int j = 0; j < kGroups; ++j) tmem_st8(tb + uint32_t(j * 8), acc[j]);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tfull[b]);
+            ++nb;
+        }
+    } else {
+        // ---------------- writers: drain lane quarter q, then the elements copies do not carry ---
+        const int q = warp - kWriter0;
+        PieceCursor pc;
+        float* shard = nullptr;
+        int64_t nb = 0;
+        for (int64_t c = blockIdx.x; c < nchunks; c += gridDim.x) {
+            if (pc.seek(segs, chunk_piece, c)) shard = shards[pc.d];
+            const ChunkView v = pc.view(c, kBulkChunk, allow_vec);
+            float* __restrict__ dst = shard + v.dst;
+            if (v.nbulk > 0) {
+                const bool whole = v.nbulk == kBulkChunk;
+                const int b = int(nb & 1);
+                if (!__all_sync(0xffffffffu, wait_bounded(&tfull[b], uint32_t((nb >> 1) & 1), timeout_ns, abort, status, 32)))
+                    break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const int sw = store_width(dst);
+                const uint32_t tb = tbase + (uint32_t(32 * q) << 16) + uint32_t(b) * kTmemBufCols;
+                // consumer warps q, q + 4, q + 8, q + 12 (< 15) park their sums in this quarter
+                for (int cw = q; cw < kBulkConsumerWarps; cw += 4) {
+                    float a[kGroups][8];
+#pragma unroll
+                    for (int j = 0; j < kGroups; ++j) tmem_ld8(tb + uint32_t(((cw >> 2) * kGroups + j) * 8), a[j]);
+                    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+                    for (int j = 0; j < kGroups; ++j) {
+                        const int64_t e = (int64_t(j) * kConsumers + cw * 32 + lane) * 8;
+                        if (whole || e + 8 <= v.nbulk) store8(dst + e, a[j], sw);
+                    }
+                }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[b]);
+                ++nb;
+            }
+            // valid elements not carried by the copies, then padding
+            for (int64_t e = v.nbulk + q * 32 + lane; e < v.n; e += kTmemWriters * 32)
+                dst[e] = (e < v.nvalid) ? sum_scalar(grads, R, P, v.p, v.src + e) : 0.0f;
+        }
+    }
+
+    // everyone is done with TMEM before the allocating warp frees it
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (warp == kWriter0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tbase), "r"(kTmemCols) : "memory");
+}
+
 }  // namespace
 
 size_t bulk_smem_bytes(int R, int stages) {
@@ -396,6 +652,23 @@ cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, const int32_t* chunk_p
     const int grid = int(std::min<int64_t>(ctas, nchunks));
     reduce_scatter_bulk_kernel<<<grid, kBulkThreads, smem, stream>>>(segs, chunk_piece, nchunks, grads, shards, R, P,
                                                                      allow_vec, stages, status, timeout_ns, inject);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_scatter_tmem(const RsSeg* segs, const int32_t* chunk_piece, int64_t nchunks,
+                                       const uint16_t* const* grads, float* const* shards, int R, int P,
+                                       int allow_vec, int ctas, int* status, uint64_t timeout_ns, int inject,
+                                       cudaStream_t stream) {
+    if (nchunks <= 0) return cudaSuccess;
+    const int stages = bulk_stages(R);
+    if (stages < 2) return cudaErrorInvalidValue;
+    const size_t smem = bulk_smem_bytes(R, stages);
+    cudaError_t e = cudaFuncSetAttribute(reduce_scatter_tmem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    if (e != cudaSuccess) return e;
+    const int grid = int(std::min<int64_t>(ctas, nchunks));
+    reduce_scatter_tmem_kernel<<<grid, kTmemThreads, smem, stream>>>(segs, chunk_piece, nchunks, grads, shards, R,
+                                                                     P, allow_vec, stages, status, timeout_ns, inject);
     return cudaGetLastError();
 }
 

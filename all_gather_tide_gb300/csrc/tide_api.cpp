@@ -285,6 +285,16 @@ bool use_bulk(const tide_group* g, bool aligned) {
     return g->rs_variant != TIDE_RS_REGISTER;
 }
 
+// Which bulk-copy kernel: the TMEM-staged one unless TIDE_RS_BULK asks for the original.  Measured
+// on GB300 over every workload: at 16 CTAs the staged kernel moves 5-22 % more (70B layer 2.17
+// against 1.78 TB/s; Wan R = 64, where the R rows already spread the stores, 2.14 against 2.11), at
+// the default grid -1 to +2 % (70B 7.17 against 7.07).
+using RsBulkLaunch = cudaError_t (*)(const tide::RsSeg*, const int32_t*, int64_t, const uint16_t* const*,
+                                     float* const*, int, int, int, int, int*, uint64_t, int, cudaStream_t);
+RsBulkLaunch rs_bulk_launcher(const tide_group* g) {
+    return g->rs_variant == TIDE_RS_BULK ? tide::launch_reduce_scatter_bulk : tide::launch_reduce_scatter_tmem;
+}
+
 }  // namespace
 
 extern "C" {
@@ -488,9 +498,9 @@ int tide_reduce_scatter(tide_group_t g, const void* const* grads, void* const* s
     cudaError_t e;
     if (use_bulk(g, aligned)) {
         const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, true);
-        e = tide::launch_reduce_scatter_bulk(g->d_rs_bulk, g->d_rs_bulk_piece, g->plan.rs_bulk_chunks, gp, sp,
-                                             R, P, 1, ctas, g->d_status, g->timeout_ns,
-                                             (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
+        auto* launch = rs_bulk_launcher(g);
+        e = launch(g->d_rs_bulk, g->d_rs_bulk_piece, g->plan.rs_bulk_chunks, gp, sp, R, P, 1, ctas, g->d_status,
+                   g->timeout_ns, (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
     } else {
         const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, false);
         e = tide::launch_reduce_scatter(g->d_rs, int(g->plan.rs.size()), g->d_rs_piece, g->plan.rs_chunks, gp, sp,
@@ -525,10 +535,10 @@ int tide_reduce_scatter_slots(tide_group_t g, int32_t d, const void* const* slot
     const auto* gp = reinterpret_cast<const uint16_t* const*>(dev);
     auto* sp = reinterpret_cast<float* const*>(dev + R);
     const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, true);
-    cudaError_t e = tide::launch_reduce_scatter_bulk(g->d_rs_slots + size_t(d) * size_t(P), g->d_rs_slot_piece,
-                                                     g->plan.rs_slot_chunks, gp, sp, R, 1, aligned ? 1 : 0, ctas,
-                                                     g->d_status, g->timeout_ns,
-                                                     (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
+    auto* launch = rs_bulk_launcher(g);
+    cudaError_t e = launch(g->d_rs_slots + size_t(d) * size_t(P), g->d_rs_slot_piece, g->plan.rs_slot_chunks, gp, sp,
+                           R, 1, aligned ? 1 : 0, ctas, g->d_status, g->timeout_ns,
+                           (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
     if (e != cudaSuccess) return cuda_fail(e);
     return finish_slot(g, k, st);
 }
@@ -639,7 +649,7 @@ int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* p
 }
 
 int tide_group_set_rs_variant(tide_group_t g, int32_t variant) {
-    if (!g || variant < TIDE_RS_AUTO || variant > TIDE_RS_BULK) return TIDE_EINVAL;
+    if (!g || variant < TIDE_RS_AUTO || variant > TIDE_RS_TMEM) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);
     g->rs_variant = variant;
     return TIDE_OK;

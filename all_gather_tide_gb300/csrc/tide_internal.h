@@ -122,6 +122,12 @@ cudaError_t launch_reduce_scatter_bulk(const RsSeg* segs, const int32_t* chunk_p
                                        const uint16_t* const* grads,
                                        float* const* shards, int R, int P, int allow_vec, int ctas, int* status,
                                        uint64_t timeout_ns, int inject, cudaStream_t stream);
+// TMEM-staged variant of the bulk-copy kernel (same tables, same results): the consumers hand
+// their sums to Tensor Memory and separate writer warps store them.
+cudaError_t launch_reduce_scatter_tmem(const RsSeg* segs, const int32_t* chunk_piece, int64_t nchunks,
+                                       const uint16_t* const* grads, float* const* shards, int R, int P,
+                                       int allow_vec, int ctas, int* status, uint64_t timeout_ns, int inject,
+                                       cudaStream_t stream);
 size_t ag_bulk_smem_bytes();
 cudaError_t launch_all_gather_bulk(const AgSeg* segs, int nsegs, int64_t nchunks, const uint16_t* const* shards,
                                    uint16_t* const* params, int ctas, int* status, uint64_t timeout_ns,

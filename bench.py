@@ -250,7 +250,7 @@ def run_tide(args, rank, world, local_rank):
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
     G.set_ctas(args.rs_ctas, args.ag_ctas)
     G.set_rs_variant({"auto": tide.TIDE_RS_AUTO, "register": tide.TIDE_RS_REGISTER,
-                      "bulk": tide.TIDE_RS_BULK}[args.rs_variant])
+                      "bulk": tide.TIDE_RS_BULK, "tmem": tide.TIDE_RS_TMEM}[args.rs_variant])
     G.set_ag_variant({"auto": tide.TIDE_AG_AUTO, "register": tide.TIDE_AG_REGISTER,
                       "bulk": tide.TIDE_AG_BULK}[args.ag_variant])
     if args.ce_lanes:
@@ -325,7 +325,9 @@ def run_tide(args, rank, world, local_rank):
     legs["all_gather_register"] = time_ag_variant(G, buf, stream, b_ag, max(3, args.steps), args, "register")
     # the summing step always runs the bulk-copy kernel: the caller's count, else one CTA per SM
     slot_ctas = args.rs_ctas or torch.cuda.get_device_properties(dev).multi_processor_count
-    legs["reduce_scatter_slots"] = time_rs_slots(G, g, buf, S, stream, max(3, args.steps), slot_ctas)
+    legs["reduce_scatter_slots"] = time_rs_slots(G, g, buf, S, stream, max(3, args.steps), slot_ctas,
+                                                 "reduce_scatter_bulk_kernel" if args.rs_variant == "bulk"
+                                                 else "reduce_scatter_tmem_kernel")
     for leg in legs.values():
         leg["frac_of_peak"] = leg["gbs"] / peak
 
@@ -350,8 +352,10 @@ def run_tide(args, rank, world, local_rank):
     }
     if args.rs_variant == "register":
         rs_kernel, rs_srcs = "reduce_scatter_kernel", ["rs_kernel.cu", "tide_internal.h"]
-    else:  # 16-byte aligned torch allocations: the bulk-copy kernel runs
+    elif args.rs_variant == "bulk":
         rs_kernel, rs_srcs = "reduce_scatter_bulk_kernel", ["rs_bulk_kernel.cu", "tide_internal.h"]
+    else:  # 16-byte aligned torch allocations: the TMEM-staged bulk-copy kernel runs
+        rs_kernel, rs_srcs = "reduce_scatter_tmem_kernel", ["rs_bulk_kernel.cu", "tide_internal.h"]
     legs["reduce_scatter"]["kernel"] = rs_kernel
     traffic = recorded_traffic(rs_kernel, g.name, rs_srcs)
     out["roofline"] = {"bound": "hbm", "kernel": rs_kernel, "achieved": legs["reduce_scatter"]["gbs"],
@@ -499,7 +503,7 @@ def slot_reuse(G, g, buf, S, U, stream):
             "grad_bytes_released_after_staging": grad_bytes, "slot_bytes": g.R * g.R * S * 2}
 
 
-def time_rs_slots(G, g: Group, buf, S: int, stream, iters: int, ctas: int, d: int = 0) -> dict:
+def time_rs_slots(G, g: Group, buf, S: int, stream, iters: int, ctas: int, kernel: str, d: int = 0) -> dict:
     """The reduce-scatter as destination d would run it on R GPUs: the exchange that fills its R
     staging slots (tide_stage_slices: copy-engine copies, here device to device) and the summing
     step (tide_reduce_scatter_slots) into d's fp32 shard, each timed on its own.  Bytes of the sum:
@@ -542,7 +546,7 @@ def time_rs_slots(G, g: Group, buf, S: int, stream, iters: int, ctas: int, d: in
     avg = statistics.mean(ms)
     del slots, out, slot_list
     return {"gbs": nbytes / (avg * 1e-3) / 1e9, "ms": avg, "ms_median": statistics.median(ms), "bytes": nbytes,
-            "destination": d, "ctas": ctas, "kernel": "reduce_scatter_bulk_kernel",
+            "destination": d, "ctas": ctas, "kernel": kernel,
             "what": "tide_reduce_scatter_slots: one destination's R staging slots summed into its fp32 shard",
             "exchange": {"gbs": valid * 4 / (sms * 1e-3) / 1e9, "ms": sms, "bytes": valid * 4,
                          "what": "tide_stage_slices: the R*P copies that fill the slots, copy engines over the "
@@ -800,16 +804,22 @@ def sm_mixed(dev, stream, ctas=16):
     buf.fill_(0x3C00_3C00)
     st = torch.empty(ns, dtype=torch.uint8, device=dev)
     out = torch.zeros(3, dtype=torch.int64, device=dev)
+    # (mode, copy bytes, stages, reading warps, writing warps, reads?, burst rows, burst vectors)
     cases = [("writes only", 73728, 3, 1, 14, False), ("writes only", 73728, 3, 1, 4, False),
              ("reads only", 73728, 3, 15, 0, True), ("reads and writes", 73728, 3, 14, 1, True),
              ("reads and writes", 73728, 3, 13, 2, True), ("reads and writes", 73728, 3, 12, 3, True),
              ("reads and writes", 73728, 3, 11, 4, True),
              ("reads and writes", 73728, 3, 8, 7, True), ("reads only", 46080, 5, 15, 0, True),
-             ("reads and writes", 46080, 5, 14, 1, True)]
+             ("reads and writes", 46080, 5, 14, 1, True),
+             # the reading threads themselves store 6 (10) 32-byte vectors after every 8 landed copies:
+             # the reduce-scatter's 1:4 ratio and its store pattern at 45 KB (72 KB) copies
+             ("reads with burst writes", 46080, 5, 15, 0, True, 8, 6),
+             ("reads with burst writes", 73728, 3, 15, 0, True, 8, 10)]
+    cases = [c if len(c) == 8 else c + (0, 0) for c in cases]
 
-    def launch(copy, stages, cons, stw, reads):
+    def launch(copy, stages, cons, stw, reads, brows=0, bvecs=0):
         bulk = nb // copy * copy if reads else 0
-        tide.tide_probe_mixed(buf, bulk, st, ns, ctas, copy, stages, cons, stw, out, stream)
+        tide.tide_probe_mixed(buf, bulk, st, ns, ctas, copy, stages, cons, stw, out, stream, brows, bvecs)
         return bulk
 
     with torch.cuda.stream(stream):
@@ -817,18 +827,19 @@ def sm_mixed(dev, stream, ctas=16):
             launch(73728, 3, 15, 0, True)
     torch.cuda.synchronize()
     rows = []
-    for name, copy, stages, cons, stw, reads in cases:
+    for name, copy, stages, cons, stw, reads, brows, bvecs in cases:
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         with torch.cuda.stream(stream):
-            launch(copy, stages, cons, stw, reads)
+            launch(copy, stages, cons, stw, reads, brows, bvecs)
             out[2].zero_()
             ev[0].record(stream)
-            n = sum(launch(copy, stages, cons, stw, reads) for _ in range(3))
+            n = sum(launch(copy, stages, cons, stw, reads, brows, bvecs) for _ in range(3))
             ev[1].record(stream)
         torch.cuda.synchronize()
         s = ev[0].elapsed_time(ev[1]) * 1e-3
         w = int(out[2].item())
         rows.append({"mode": name, "copy_bytes": copy, "stages": stages, "consumer_warps": cons, "st_warps": stw,
+                     "burst_rows": brows, "burst_vecs": bvecs,
                      "read_gbs_per_sm": n / s / 1e9 / ctas, "write_gbs_per_sm": w / s / 1e9 / ctas})
     assert int(out[1].item()) == 0, "a probe wait expired"
     del buf, st
@@ -841,7 +852,7 @@ def mixed_bound(rows, write_per_read: float):
     read, interpolated between the probe's measured points of the 72 KB x 3 geometry (reads alone,
     then 1, 2, 3, 4 and 7 writer warps), linear in the ratio; None outside the measured range."""
     pts = sorted((r["write_gbs_per_sm"] / r["read_gbs_per_sm"], r["read_gbs_per_sm"]) for r in rows
-                 if r["copy_bytes"] == 73728 and r["read_gbs_per_sm"] > 0)
+                 if r["copy_bytes"] == 73728 and r["read_gbs_per_sm"] > 0 and not r.get("burst_rows"))
     for (x0, r0), (x1, r1) in zip(pts, pts[1:]):
         if x0 <= write_per_read <= x1:
             rd = r0 + (r1 - r0) * (write_per_read - x0) / (x1 - x0) if x1 > x0 else min(r0, r1)
@@ -857,7 +868,8 @@ def cta_sweep(G, buf, stream, args, concurrent):
     import all_gather_tide_gb300 as tide
 
     rows = []
-    cases = [("reduce_scatter", v, n) for v in (tide.TIDE_RS_REGISTER, tide.TIDE_RS_BULK) for n in args.sweep_rs]
+    cases = [("reduce_scatter", v, n) for v in (tide.TIDE_RS_REGISTER, tide.TIDE_RS_BULK, tide.TIDE_RS_TMEM)
+             for n in args.sweep_rs]
     cases += [("all_gather_sm", v, n) for v in (tide.TIDE_AG_REGISTER, tide.TIDE_AG_BULK) for n in args.sweep_ag]
     for kind, variant, n in cases:
         if kind == "reduce_scatter":
@@ -879,7 +891,7 @@ def cta_sweep(G, buf, stream, args, concurrent):
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
         c = concurrent(launch, kind, reps=2)
-        rows.append({"kind": kind, "variant": {0: "auto", 1: "register", 2: "bulk"}[variant], "ctas": n,
+        rows.append({"kind": kind, "variant": {0: "auto", 1: "register", 2: "bulk", 3: "tmem"}[variant], "ctas": n,
                      "alone_ms": ms / reps, "gbs": nbytes / (ms * 1e-3) / 1e9,
                      "gemm_slowdown_pct": c["slowdown_pct"], "gemms": c["gemms_started_inside"]})
     G.set_ctas(args.rs_ctas, args.ag_ctas)
@@ -1005,8 +1017,9 @@ def probes(G, buf, stream, dev, args):
 
     # Table 4 / Table 5 for several reduce-scatter configurations, and for the copy-engine
     # placement (8 placements back to back, so the victims and probes overlap it)
-    configs = [("reduce_scatter", "bulk", 0), ("reduce_scatter", "bulk", 16), ("reduce_scatter", "bulk", 4),
-               ("reduce_scatter", "register", 16), ("all_gather_ce", "1d", 1), ("all_gather_ce", "1d", 8),
+    configs = [("reduce_scatter", "tmem", 0), ("reduce_scatter", "tmem", 16), ("reduce_scatter", "tmem", 4),
+               ("reduce_scatter", "bulk", 16), ("reduce_scatter", "register", 16), ("all_gather_ce", "1d", 1),
+               ("all_gather_ce", "1d", 8),
                ("all_gather_ce", "2d", 1)]
     G2 = tide.Group(G.R, list(zip(G.rows, G.row_len)), tide.TIDE_FLAG_CE_2D)
     G2.set_ce_bands(1)  # the paper's form: one strided copy per parameter
@@ -1015,7 +1028,8 @@ def probes(G, buf, stream, dev, args):
     for coll, variant, n_ in configs:
         if coll == "reduce_scatter":
             G.set_ctas(n_, 0)
-            G.set_rs_variant(tide.TIDE_RS_BULK if variant == "bulk" else tide.TIDE_RS_REGISTER)
+            G.set_rs_variant({"bulk": tide.TIDE_RS_BULK, "tmem": tide.TIDE_RS_TMEM,
+                              "register": tide.TIDE_RS_REGISTER}[variant])
             rs = lambda: G.reduce_scatter(buf.grads, buf.shard_list, stream)
             row = {"collective": coll, "variant": variant, "ctas": n_ or G.get_ctas()[0]}
         else:
@@ -1346,7 +1360,7 @@ def main():
     ap.add_argument("--scale", type=int, default=1, help="divide every dimension by this (profiling cases)")
     ap.add_argument("--rs-ctas", type=int, default=0)
     ap.add_argument("--ag-ctas", type=int, default=0)
-    ap.add_argument("--rs-variant", choices=["auto", "register", "bulk"], default="auto")
+    ap.add_argument("--rs-variant", choices=["auto", "register", "bulk", "tmem"], default="auto")
     ap.add_argument("--ag-variant", choices=["auto", "register", "bulk"], default="auto")
     ap.add_argument("--ce-lanes", type=int, default=0, help="copy-engine streams (0 = library default)")
     ap.add_argument("--ce-lanes-sweep", type=int, nargs="*", default=[])

@@ -222,14 +222,17 @@ int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *p
                        void *stream);
 
 /* ---- reduce-scatter kernel variants and device-side waits --------------------------------- */
-#define TIDE_RS_AUTO 0     /* bulk-copy path when every gradient pointer is 16-byte aligned, else register path */
+#define TIDE_RS_AUTO 0     /* TIDE_RS_TMEM when every gradient pointer is 16-byte aligned, else register path */
 #define TIDE_RS_REGISTER 1 /* 16-byte register loads of 8 ranks in flight per thread, 2 CTAs per SM */
 #define TIDE_RS_BULK 2     /* 45 KB bulk asynchronous copies, one rank row per stage, 1 CTA per SM */
+#define TIDE_RS_TMEM 3     /* the bulk path with its sums staged in Tensor Memory and stored by separate
+                              writer warps (needs 16-byte aligned gradients like TIDE_RS_BULK); each CTA
+                              holds its SM's whole Tensor Memory (512 columns) while it runs */
 
 /*
  * Chooses the reduce-scatter kernel (Fig. 2b step 5 / Fig. 6a: sums formed by a bounded number of
- * CTAs fed by bulk copies).  Both give identical bits.  The bulk path needs 16-byte aligned
- * pointers; otherwise the register path runs.
+ * CTAs fed by bulk copies), for tide_reduce_scatter and tide_reduce_scatter_slots.  All give
+ * identical bits.  The bulk paths need 16-byte aligned pointers; otherwise the register path runs.
  */
 int tide_group_set_rs_variant(tide_group_t g, int32_t variant);
 
@@ -259,7 +262,8 @@ int tide_group_set_wait_timeout(tide_group_t g, uint64_t timeout_ns);
 
 /* Reads the group's device status word (0 = no wait expired; 1 = a reduce-scatter consumer wait
  * expired, 2 = a reduce-scatter producer wait expired, 4 = draining copies after an abort expired,
- * 8 = a placement load wait expired) and clears it.
+ * 8 = a placement load wait expired, 16 / 32 = TIDE_RS_TMEM: a consumer's wait for a drained Tensor
+ * Memory buffer / a writer's wait for a filled one expired) and clears it.
  * Synchronous: copies from the device. */
 int tide_group_device_status(tide_group_t g, int32_t *status);
 
@@ -394,15 +398,19 @@ int tide_probe_ingest(const void *buf, int64_t bulk_bytes, int64_t ldg_bytes, in
  * word of each landed copy; buf 256-byte aligned) while `st_warps` warps per CTA write 32-byte
  * vectors into the CTA's equal share of [st_buf, st_buf + st_bytes) (st_buf 32-byte aligned,
  * st_bytes a multiple of 32), cycling over it until that CTA's reads have landed; with bulk_bytes
- * == 0 they write their share once.  The written values are a pattern of no meaning; nothing else
- * is written.  1 + consumer_warps + st_warps <= 16.
+ * == 0 they write their share once.  With burst_rows > 0 the reading warps also write, as a
+ * reduce-scatter stores its sums after the last rank's row: after every burst_rows landed copies
+ * each reading thread stores burst_vecs 32-byte vectors (adjacent threads to adjacent vectors) into
+ * the CTA's share, cycling over it.  The written values are a pattern of no meaning (the checked
+ * pattern of the dedicated writers holds only when burst_rows == 0); nothing else is written.
+ * 1 + consumer_warps + st_warps <= 16.
  * out (device, 3 uint64): out[0] ^= checksum of what was read, out[1] |= 1 if a wait (1 s bound)
  * expired, 2 if copies were still landing 1 s after the last issue, 4 if the writers stopped at
  * their 2 s bound; out[2] += bytes written.  TIDE_EINVAL on bad arguments.
  */
 int tide_probe_mixed(const void *buf, int64_t bulk_bytes, void *st_buf, int64_t st_bytes, int32_t ctas,
-                     int32_t copy_bytes, int32_t stages, int32_t consumer_warps, int32_t st_warps, uint64_t *out,
-                     void *stream);
+                     int32_t copy_bytes, int32_t stages, int32_t consumer_warps, int32_t st_warps, int32_t burst_rows,
+                     int32_t burst_vecs, uint64_t *out, void *stream);
 
 /* ---- errors ------------------------------------------------------------------------------ */
 const char *tide_strerror(int status);

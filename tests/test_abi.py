@@ -124,9 +124,11 @@ def test_probe_argument_checks_before_cuda(tide):
                    ("cons", -1), ("ldgw", 8), ("ldg", 33), ("out", 0)):
         args = dict(ok, **{k: bad})
         assert L.tide_probe_ingest(*args.values(), None) == tide.TIDE_EINVAL, (k, bad)
-    ok = dict(buf=256, bulk=1 << 20, st=512, stb=1 << 20, ctas=16, copy=73728, stages=3, cons=11, stw=4, out=16)
+    ok = dict(buf=256, bulk=1 << 20, st=512, stb=1 << 20, ctas=16, copy=73728, stages=3, cons=11, stw=4, br=8, bv=6,
+              out=16)
     for k, bad in (("buf", 0), ("buf", 272), ("st", 0), ("st", 528), ("stb", 33), ("ctas", 0), ("copy", 46081),
-                   ("stages", 4), ("cons", 0), ("stw", 5), ("stw", -1), ("out", 0)):
+                   ("stages", 4), ("cons", 0), ("stw", 5), ("stw", -1), ("br", -1), ("bv", -1), ("stb", 32 * 15),
+                   ("out", 0)):
         args = dict(ok, **{k: bad})
         assert L.tide_probe_mixed(*args.values(), None) == tide.TIDE_EINVAL, (k, bad)
 

@@ -173,6 +173,18 @@ def test_reduce_scatter_bulk_matches_oracle(tide, g):
     run_rs(tide, g, variant=tide.TIDE_RS_BULK)
 
 
+@pytest.mark.parametrize("g", reduced_groups(), ids=_ids(reduced_groups()))
+def test_reduce_scatter_tmem_matches_oracle(tide, g):
+    run_rs(tide, g, variant=tide.TIDE_RS_TMEM)
+
+
+@pytest.mark.parametrize("ctas", [1, 3, 16, 152, 1000])
+def test_reduce_scatter_tmem_cta_counts(tide, ctas):
+    run_rs(tide, group("qwen3moe").scaled(16), ctas=ctas, variant=tide.TIDE_RS_TMEM)
+    run_rs(tide, group("wan_r64").scaled(16), ctas=ctas, variant=tide.TIDE_RS_TMEM)
+    run_rs(tide, edge_groups()[3], ctas=ctas, variant=tide.TIDE_RS_TMEM)
+
+
 @pytest.mark.parametrize("ctas", [1, 3, 16, 24, 152])
 def test_reduce_scatter_bulk_cta_counts(tide, ctas):
     run_rs(tide, group("qwen3moe").scaled(16), ctas=ctas, variant=tide.TIDE_RS_BULK)
@@ -201,7 +213,7 @@ def _special_grads(g, seed, pool):
     return out
 
 
-@pytest.mark.parametrize("variant", [1, 2], ids=["register", "bulk"])
+@pytest.mark.parametrize("variant", [1, 2, 3], ids=["register", "bulk", "tmem"])
 def test_special_values(tide, variant):
     """Signed zeros, bf16 subnormals (fp32 subnormals after widening), the largest finite values
     (whose sums overflow to infinity under round-to-nearest), infinities and NaN: finite results
@@ -227,13 +239,15 @@ def test_special_values(tide, variant):
         G.close()
 
 
-def test_bulk_wait_timeout_reports_status_and_context_survives(tide):
+@pytest.mark.parametrize("variant", [2, 3], ids=["bulk", "tmem"])
+def test_bulk_wait_timeout_reports_status_and_context_survives(tide, variant):
     """A producer that never signals (test hook) makes the bounded waits expire (the consumers'
-    on data that never arrives, the producer's on stages never freed): the kernel returns, the
-    status word records the first wait that gave up, and the next call runs normally."""
+    on data that never arrives, the producer's on stages never freed, the writers' on sums never
+    handed over): the kernel returns, the status word records the first wait that gave up, and the
+    next call runs normally."""
     g = group("llama70b").scaled(64)
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
-    G.set_rs_variant(tide.TIDE_RS_BULK)
+    G.set_rs_variant(variant)
     G.set_ctas(8, 0)
     G.set_wait_timeout(50_000_000)  # 50 ms
     grads = [[rng.grad_bits(g, r, p, device="cuda").view(torch.bfloat16) for p in range(g.P)] for r in range(g.R)]
@@ -241,8 +255,8 @@ def test_bulk_wait_timeout_reports_status_and_context_survives(tide):
     G.set_debug(tide.TIDE_DEBUG_STALL_PRODUCER)
     G.reduce_scatter(grads, list(shards))
     torch.cuda.synchronize()
-    # both sides wait on stages nobody fills or frees; whichever bound expires first is recorded
-    assert G.device_status() in (1, 2)
+    # every side waits on something nobody provides; whichever bound expires first is recorded
+    assert G.device_status() in ((1, 2) if variant == 2 else (1, 2, 32))
     G.set_debug(0)
     G.set_wait_timeout(0)
     G.reduce_scatter(grads, list(shards))
@@ -529,13 +543,15 @@ def _sample_positions(lay, seed, n=3000):
     return np.asarray(d, np.int64), np.asarray(j, np.int64)
 
 
-FULL_CASES = [(n, 0) for n in FULL] + [("llama70b", 16), ("qwen3moe", 16), ("wan_r64", 24)]
+FULL_CASES = [(n, 0, 0) for n in FULL] + [("llama70b", 16, 0), ("qwen3moe", 16, 0), ("wan_r64", 24, 0),
+                                          ("llama70b", 0, 3), ("llama70b", 16, 3), ("qwen3moe", 16, 3)]
 
 
-@pytest.mark.parametrize("name,ctas", FULL_CASES, ids=[f"{n}-ctas{c or 'default'}" for n, c in FULL_CASES])
-def test_full_size_reduce_scatter(tide, name, ctas):
+@pytest.mark.parametrize("name,ctas,variant", FULL_CASES,
+                         ids=[f"{n}-ctas{c or 'default'}{'-tmem' if v == 3 else ''}" for n, c, v in FULL_CASES])
+def test_full_size_reduce_scatter(tide, name, ctas, variant):
     """Default CTAs = the benchmark's step; capped CTAs = the automatic bulk-copy path the
-    interference harness times."""
+    interference harness times; variant 3 = the TMEM-staged kernel."""
     g = group(name)
     lay = oracle.plan(g.R, g.rows, g.row_len)
     grads = [[rng.grad_bits(g, r, p, device="cuda").view(torch.bfloat16) for p in range(g.P)] for r in range(g.R)]
@@ -543,6 +559,7 @@ def test_full_size_reduce_scatter(tide, name, ctas):
     shards.view(torch.int32).fill_(F32_SENTINEL)
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
     G.set_ctas(ctas, 0)
+    G.set_rs_variant(variant)
     G.reduce_scatter(grads, list(shards))
     torch.cuda.synchronize()
     assert G.device_status() == 0
@@ -726,13 +743,14 @@ def fill_slots(g, lay, grads, d, slots):
         slots[c.src_rank][c.dst_off:c.dst_off + c.elems].copy_(grads[c.src_rank][c.param][c.src_off:c.src_off + c.elems])
 
 
-def run_rs_slots(tide, g, dests=None, ctas=0, misalign=False, flags=0, library_staging=False, lanes=0):
+def run_rs_slots(tide, g, dests=None, ctas=0, misalign=False, flags=0, library_staging=False, lanes=0, variant=0):
     lay = oracle.plan(g.R, g.rows, g.row_len)
     host = rng.group_grads(g)
     want = oracle.reduce_scatter(lay, [[t.numpy().view(np.uint16) for t in row] for row in host])
     grads = [[t.cuda().view(-1) for t in row] for row in host]
     G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
     G.set_ctas(ctas, 0)
+    G.set_rs_variant(variant)
     if lanes:
         G.set_ce_lanes(lanes)
     off = 1 if misalign else 0
@@ -780,6 +798,13 @@ def test_stage_slices_then_sum_matches_oracle(tide, g):
 def test_stage_slices_lanes_stay_stream_ordered(tide, lanes):
     run_rs_slots(tide, group("qwen3moe").scaled(16), [0, 3, 7], library_staging=True, lanes=lanes)
     run_rs_slots(tide, edge_groups()[2], None, library_staging=True, lanes=lanes, misalign=True)
+
+
+@pytest.mark.parametrize("g", [group("tiny"), group("llama70b").scaled(32), group("wan_r64").scaled(16)],
+                         ids=lambda g: g.name)
+def test_reduce_scatter_slots_tmem(tide, g):
+    run_rs_slots(tide, g, _slot_dests(g), variant=tide.TIDE_RS_TMEM)
+    run_rs_slots(tide, g, _slot_dests(g), ctas=16, variant=tide.TIDE_RS_TMEM)
 
 
 @pytest.mark.parametrize("ctas", [1, 3, 16, 1000])

@@ -109,3 +109,21 @@ def test_mixed_probe_reads_every_byte_while_writing(tide, consumers, st_warps):
     assert o[1] == 0
     assert np.uint32(o[0] & 0xFFFFFFFF) == want
     assert (o[2] > 0) == (st_warps > 0)
+
+
+def test_mixed_probe_burst_writes_count(tide):
+    """Reading threads that also write in bursts (the reduce-scatter's store pattern): every byte is
+    still read, and the bytes written are exactly the bursts the CTAs' copies call for."""
+    copy, stages, cons, ctas, rows, vecs = 46080, 5, 15, 16, 8, 6
+    nchunk = (64 << 20) // copy
+    bulk = nchunk * copy
+    buf = torch.randint(-2**31, 2**31 - 1, (bulk // 4 + 64,), dtype=torch.int32, device="cuda")
+    st = torch.empty(16 << 20, dtype=torch.uint8, device="cuda")
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    tide.tide_probe_mixed(buf, bulk, st, st.numel(), ctas, copy, stages, cons, 0, out, burst_rows=rows, burst_vecs=vecs)
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    per_cta = [len(range(b, nchunk, ctas)) for b in range(ctas)]
+    want_written = sum(k // rows for k in per_cta) * cons * 32 * vecs * 32
+    assert o[1] == 0 and o[2] == want_written
+    assert np.uint32(o[0] & 0xFFFFFFFF) == np.bitwise_xor.reduce(buf.cpu().numpy().view(np.uint32)[: bulk // 4])
