@@ -286,9 +286,9 @@ bool use_bulk(const tide_group* g, bool aligned) {
 }
 
 // Which bulk-copy kernel: the TMEM-staged one unless TIDE_RS_BULK asks for the original.  Measured
-// on GB300 over every workload: at 16 CTAs the staged kernel moves 5-22 % more (70B layer 2.17
-// against 1.78 TB/s; Wan R = 64, where the R rows already spread the stores, 2.14 against 2.11), at
-// the default grid -1 to +2 % (70B 7.17 against 7.07).
+// on GB300 over every workload: at 16 CTAs the staged kernel moves 1-23 % more (70B layer 2.18
+// against 1.79 TB/s; Wan R = 64, where the R rows already spread the stores, 2.13 against 2.12), at
+// the default grid within +-1.5 % (70B 7.09 against 7.00).
 using RsBulkLaunch = cudaError_t (*)(const tide::RsSeg*, const int32_t*, int64_t, const uint16_t* const*,
                                      float* const*, int, int, int, int, int*, uint64_t, int, cudaStream_t);
 RsBulkLaunch rs_bulk_launcher(const tide_group* g) {
