@@ -786,11 +786,12 @@ def sm_ingest(dev, stream, full=False, ctas=16):
         gbs = n / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
         rows.append({"mode": name, "copy_bytes": copy, "stages": stages, "consumer_warps": cons,
                      "ldg_warps": ldgw, "bulk_fraction": f, "gbs": gbs, "gbs_per_sm": gbs / ctas})
-    assert int(out[1].item()) == 0, "a probe wait expired"
+    flags = int(out[1].item())  # nonzero: a bounded probe wait expired (the rates are then suspect)
     del buf
     torch.cuda.empty_cache()
     best = max(rows, key=lambda r: r["gbs_per_sm"])
-    return {"ctas": ctas, "rows": rows, "ceiling_gbs_per_sm": best["gbs_per_sm"], "ceiling_mode": best["mode"]}
+    return {"ctas": ctas, "rows": rows, "ceiling_gbs_per_sm": best["gbs_per_sm"], "ceiling_mode": best["mode"],
+            "probe_error_flags": flags}
 
 
 def sm_mixed(dev, stream, ctas=16):
@@ -841,10 +842,10 @@ def sm_mixed(dev, stream, ctas=16):
         rows.append({"mode": name, "copy_bytes": copy, "stages": stages, "consumer_warps": cons, "st_warps": stw,
                      "burst_rows": brows, "burst_vecs": bvecs,
                      "read_gbs_per_sm": n / s / 1e9 / ctas, "write_gbs_per_sm": w / s / 1e9 / ctas})
-    assert int(out[1].item()) == 0, "a probe wait expired"
+    flags = int(out[1].item())  # nonzero: a bounded probe wait expired (the rates are then suspect)
     del buf, st
     torch.cuda.empty_cache()
-    return {"ctas": ctas, "rows": rows}
+    return {"ctas": ctas, "rows": rows, "probe_error_flags": flags}
 
 
 def mixed_bound(rows, write_per_read: float):
