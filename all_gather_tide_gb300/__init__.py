@@ -71,6 +71,7 @@ SIGNATURES = {
     "tide_group_set_ce_lanes": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "tide_group_set_ce_bands": (ctypes.c_int, [_vp, ctypes.c_int32]),
     "tide_group_ag_kernel": (ctypes.c_int, [_vp, _i32p]),
+    "tide_group_rs_kernel": (ctypes.c_int, [_vp, _i32p]),
     "tide_group_set_wait_timeout": (ctypes.c_int, [_vp, ctypes.c_uint64]),
     "tide_group_device_status": (ctypes.c_int, [_vp, _i32p]),
     "tide_group_set_debug": (ctypes.c_int, [_vp, ctypes.c_uint32]),
@@ -273,6 +274,12 @@ def tide_group_ag_kernel(g: int) -> int:
     return v.value
 
 
+def tide_group_rs_kernel(g: int) -> int:
+    v = ctypes.c_int32()
+    _check(lib().tide_group_rs_kernel(g, ctypes.byref(v)), "tide_group_rs_kernel")
+    return v.value
+
+
 def tide_group_set_ce_lanes(g: int, lanes: int) -> None:
     _check(lib().tide_group_set_ce_lanes(g, lanes), "tide_group_set_ce_lanes")
 
@@ -428,6 +435,9 @@ class Group:
 
     def ag_kernel(self) -> int:
         return tide_group_ag_kernel(self.handle)
+
+    def rs_kernel(self) -> int:
+        return tide_group_rs_kernel(self.handle)
 
     def set_ce_lanes(self, lanes: int) -> None:
         tide_group_set_ce_lanes(self.handle, lanes)

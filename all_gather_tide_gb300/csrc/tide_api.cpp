@@ -655,6 +655,14 @@ int tide_group_set_rs_variant(tide_group_t g, int32_t variant) {
     return TIDE_OK;
 }
 
+int tide_group_rs_kernel(tide_group_t g, int32_t* variant) {
+    if (!g || !variant) return TIDE_EINVAL;
+    std::lock_guard<std::mutex> lock(g->mu);
+    if (!use_bulk(g, true)) *variant = TIDE_RS_REGISTER;
+    else *variant = rs_bulk_launcher(g) == tide::launch_reduce_scatter_tmem ? TIDE_RS_TMEM : TIDE_RS_BULK;
+    return TIDE_OK;
+}
+
 int tide_group_ag_kernel(tide_group_t g, int32_t* variant) {
     if (!g || !variant) return TIDE_EINVAL;
     std::lock_guard<std::mutex> lock(g->mu);

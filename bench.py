@@ -326,7 +326,7 @@ def run_tide(args, rank, world, local_rank):
     # the summing step always runs the bulk-copy kernel: the caller's count, else one CTA per SM
     slot_ctas = args.rs_ctas or torch.cuda.get_device_properties(dev).multi_processor_count
     legs["reduce_scatter_slots"] = time_rs_slots(G, g, buf, S, stream, max(3, args.steps), slot_ctas,
-                                                 "reduce_scatter_bulk_kernel" if args.rs_variant == "bulk"
+                                                 "reduce_scatter_bulk_kernel" if G.rs_kernel() == tide.TIDE_RS_BULK
                                                  else "reduce_scatter_tmem_kernel")
     for leg in legs.values():
         leg["frac_of_peak"] = leg["gbs"] / peak
@@ -350,12 +350,11 @@ def run_tide(args, rank, world, local_rank):
         "legs": legs,
         "gpu_launches": 2 * args.steps,
     }
-    if args.rs_variant == "register":
-        rs_kernel, rs_srcs = "reduce_scatter_kernel", ["rs_kernel.cu", "tide_internal.h"]
-    elif args.rs_variant == "bulk":
-        rs_kernel, rs_srcs = "reduce_scatter_bulk_kernel", ["rs_bulk_kernel.cu", "tide_internal.h"]
-    else:  # 16-byte aligned torch allocations: the TMEM-staged bulk-copy kernel runs
-        rs_kernel, rs_srcs = "reduce_scatter_tmem_kernel", ["rs_bulk_kernel.cu", "tide_internal.h"]
+    # the kernel the library runs for these (16-byte aligned, torch-allocated) gradients
+    rs_kernel, rs_srcs = {tide.TIDE_RS_REGISTER: ("reduce_scatter_kernel", ["rs_kernel.cu", "tide_internal.h"]),
+                          tide.TIDE_RS_BULK: ("reduce_scatter_bulk_kernel", ["rs_bulk_kernel.cu", "tide_internal.h"]),
+                          tide.TIDE_RS_TMEM: ("reduce_scatter_tmem_kernel", ["rs_bulk_kernel.cu", "tide_internal.h"]),
+                          }[G.rs_kernel()]
     legs["reduce_scatter"]["kernel"] = rs_kernel
     traffic = recorded_traffic(rs_kernel, g.name, rs_srcs)
     out["roofline"] = {"bound": "hbm", "kernel": rs_kernel, "achieved": legs["reduce_scatter"]["gbs"],

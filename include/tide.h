@@ -236,6 +236,11 @@ int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *p
  */
 int tide_group_set_rs_variant(tide_group_t g, int32_t variant);
 
+/* The reduce-scatter kernel tide_reduce_scatter runs on g under the current settings when every
+ * gradient pointer is 16-byte aligned: TIDE_RS_TMEM, TIDE_RS_BULK or TIDE_RS_REGISTER (resolves
+ * TIDE_RS_AUTO). */
+int tide_group_rs_kernel(tide_group_t g, int32_t *variant);
+
 #define TIDE_AG_AUTO 0     /* bulk-copy placement when every pointer is 16-byte aligned, >= 90 % of the
                               elements lie in runs with 16-byte compatible offsets, and either the CTA
                               count is capped below the SM count or the runs average >= 1 M elements;

@@ -105,6 +105,7 @@ def test_null_group_calls(tide):
     assert L.tide_group_shard_elems(None, ctypes.byref(v)) == tide.TIDE_EINVAL
     k = ctypes.c_int32()
     assert L.tide_group_ag_kernel(None, ctypes.byref(k)) == tide.TIDE_EINVAL
+    assert L.tide_group_rs_kernel(None, ctypes.byref(k)) == tide.TIDE_EINVAL
     assert L.tide_group_set_ce_bands(None, 2) == tide.TIDE_EINVAL
     assert L.tide_reduce_scatter_slots(None, 0, arr, 16, None) == tide.TIDE_EINVAL
     assert L.tide_stage_slices(None, 0, arr, arr, None) == tide.TIDE_EINVAL

@@ -389,6 +389,21 @@ def test_auto_placement_choice(tide):
     G.close()
 
 
+def test_auto_reduce_scatter_choice(tide):
+    """AUTO resolves to the TMEM-staged kernel for aligned gradients, at any CTA count and in
+    overlap mode; explicit choices are kept."""
+    g = group("llama70b").scaled(32)
+    for flags in (0, tide.TIDE_FLAG_OVERLAP):
+        G = tide.Group(g.R, list(zip(g.rows, g.row_len)), flags)
+        assert G.rs_kernel() == tide.TIDE_RS_TMEM
+        G.set_ctas(16, 0)
+        assert G.rs_kernel() == tide.TIDE_RS_TMEM
+        for v in (tide.TIDE_RS_REGISTER, tide.TIDE_RS_BULK, tide.TIDE_RS_TMEM):
+            G.set_rs_variant(v)
+            assert G.rs_kernel() == v
+        G.close()
+
+
 @pytest.mark.parametrize("variant", [0, 1, 2], ids=["auto", "register", "bulk"])
 @pytest.mark.parametrize("g", _shifted_groups(), ids=lambda g: g.name)
 def test_all_gather_any_relative_alignment(tide, g, variant):
