@@ -323,7 +323,9 @@ reduce_scatter_bulk_kernel(const RsSeg* __restrict__ segs, const int32_t* __rest
             const bool whole = v.nbulk == kBulkChunk;  // every group of the chunk is carried
             float acc[kGroups][8];
             for (int r = 0; r < R; ++r) {
-                if (!wait_bounded(&full[s], phase, timeout_ns, abort, status, 1)) return;
+                // the warp leaves only as a whole (every lane saw the stage land, or none goes on), so
+                // the __syncwarp below never waits for a lane that has returned
+                if (!__all_sync(0xffffffffu, wait_bounded(&full[s], phase, timeout_ns, abort, status, 1))) return;
                 const uint4* row = reinterpret_cast<const uint4*>(data + int64_t(s) * kBulkChunk * 2);
                 // release the stage as soon as the warp's slice is in registers, before the adds, so
                 // the producer can refill it while the adds run
