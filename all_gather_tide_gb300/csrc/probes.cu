@@ -231,7 +231,8 @@ ingest_kernel(const unsigned char* __restrict__ buf, int64_t bulk_bytes, const u
         int64_t k = 0;
         for (int64_t c = blockIdx.x; c < nchunk; c += gridDim.x, ++k) {
             const int s = int(k % stages);
-            if (!wait(&full[s], uint32_t((k / stages) & 1))) break;
+            // the warp leaves only as a whole, so its __syncwarp never waits for a lane that left
+            if (!__all_sync(0xffffffffu, wait(&full[s], uint32_t((k / stages) & 1)))) break;
             const uint4* row = reinterpret_cast<const uint4*>(data + int64_t(s) * copy_bytes);
             if (read_all) {
                 for (int i = ctid; i < words; i += consumers * 32) {
@@ -365,7 +366,8 @@ mixed_kernel(const unsigned char* __restrict__ buf, int64_t bulk_bytes, unsigned
         int64_t k = 0;
         for (int64_t c = blockIdx.x; c < nchunk; c += gridDim.x, ++k) {
             const int s = int(k % stages);
-            if (!wait(&full[s], uint32_t((k / stages) & 1))) break;
+            // the warp leaves only as a whole, so its __syncwarp never waits for a lane that left
+            if (!__all_sync(0xffffffffu, wait(&full[s], uint32_t((k / stages) & 1)))) break;
             const uint4* row = reinterpret_cast<const uint4*>(data + int64_t(s) * copy_bytes);
             for (int i = ctid; i < words; i += consumers * 32) {
                 const uint4 w = row[i];
