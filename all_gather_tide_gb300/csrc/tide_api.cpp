@@ -295,6 +295,19 @@ RsBulkLaunch rs_bulk_launcher(const tide_group* g) {
     return g->rs_variant == TIDE_RS_BULK ? tide::launch_reduce_scatter_bulk : tide::launch_reduce_scatter_tmem;
 }
 
+// Entry points return a status, never an exception: an allocation that fails (host vectors of the
+// pointer tables and plans) becomes TIDE_ENOMEM, anything else thrown (a mutex error) TIDE_EINVAL.
+template <class F>
+int no_throw(F&& f) {
+    try {
+        return f();
+    } catch (const std::bad_alloc&) {
+        return TIDE_ENOMEM;
+    } catch (...) {
+        return TIDE_EINVAL;
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -318,108 +331,112 @@ int tide_last_cuda_error(void) { return g_last_cuda_error; }
 
 int tide_plan_layout(int32_t R, int32_t P, const int64_t* rows, const int64_t* row_len, int64_t* m,
                      int64_t* s, int64_t* o, int64_t* S, int64_t* U) {
-    if (!m || !s || !o || !S || !U) return TIDE_EINVAL;
-    tide::Plan pl;
-    const int rc = tide::make_layout(R, P, rows, row_len, &pl);
-    if (rc != TIDE_OK) return rc;
-    std::copy(pl.m.begin(), pl.m.end(), m);
-    std::copy(pl.s.begin(), pl.s.end(), s);
-    std::copy(pl.o.begin(), pl.o.end(), o);
-    *S = pl.S;
-    *U = pl.U;
-    return TIDE_OK;
+    return no_throw([&]() -> int {
+        if (!m || !s || !o || !S || !U) return TIDE_EINVAL;
+        tide::Plan pl;
+        const int rc = tide::make_layout(R, P, rows, row_len, &pl);
+        if (rc != TIDE_OK) return rc;
+        std::copy(pl.m.begin(), pl.m.end(), m);
+        std::copy(pl.s.begin(), pl.s.end(), s);
+        std::copy(pl.o.begin(), pl.o.end(), o);
+        *S = pl.S;
+        *U = pl.U;
+        return TIDE_OK;
+    });
 }
 
 int tide_group_create(tide_group_t* out, int32_t R, int32_t P, const int64_t* rows, const int64_t* row_len,
                       uint32_t flags) {
-    if (!out) return TIDE_EINVAL;
-    *out = nullptr;
-    if (flags & ~kAllFlags) return TIDE_EINVAL;
-    if ((flags & TIDE_FLAG_CE_1D) && (flags & (TIDE_FLAG_CE_2D | TIDE_FLAG_CE_STRICT))) return TIDE_EINVAL;
-    *out = nullptr;
-    tide::Plan pl;
-    int rc = tide::make_layout(R, P, rows, row_len, &pl);
-    if (rc != TIDE_OK) return rc;
-    if (int64_t(R) * P > TIDE_MAX_TABLE) return TIDE_ERANGE;
-    try {
-        tide::make_work_lists(&pl);
-    } catch (const std::bad_alloc&) {
-        return TIDE_ENOMEM;
-    }
+    return no_throw([&]() -> int {
+        if (!out) return TIDE_EINVAL;
+        *out = nullptr;
+        if (flags & ~kAllFlags) return TIDE_EINVAL;
+        if ((flags & TIDE_FLAG_CE_1D) && (flags & (TIDE_FLAG_CE_2D | TIDE_FLAG_CE_STRICT))) return TIDE_EINVAL;
+        *out = nullptr;
+        tide::Plan pl;
+        int rc = tide::make_layout(R, P, rows, row_len, &pl);
+        if (rc != TIDE_OK) return rc;
+        if (int64_t(R) * P > TIDE_MAX_TABLE) return TIDE_ERANGE;
+        try {
+            tide::make_work_lists(&pl);
+        } catch (const std::bad_alloc&) {
+            return TIDE_ENOMEM;
+        }
 
-    tide_group* g = new (std::nothrow) tide_group();
-    if (!g) return TIDE_ENOMEM;
-    g->plan = std::move(pl);
-    g->flags = flags;
-    if (flags & TIDE_FLAG_OVERLAP) g->ce_lanes = 1;
-    cudaError_t e = cudaGetDevice(&g->device);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g->sm_count, cudaDevAttrMultiProcessorCount, g->device);
-    if (e != cudaSuccess) {
-        release(g);
-        return cuda_fail(e);
-    }
-    const auto& rs = g->plan.rs;
-    const auto& ag = g->plan.ag;
-    e = cudaMalloc(&g->d_rs, std::max<size_t>(1, rs.size()) * sizeof(tide::RsSeg));
-    if (e == cudaSuccess) e = cudaMalloc(&g->d_ag, std::max<size_t>(1, ag.size()) * sizeof(tide::AgSeg));
-    if (e == cudaSuccess && !rs.empty())
-        e = cudaMemcpy(g->d_rs, rs.data(), rs.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
-    const auto& rsp = g->plan.rs_piece;
-    if (e == cudaSuccess && !rsp.empty()) {
-        e = cudaMalloc(&g->d_rs_piece, rsp.size() * sizeof(int32_t));
-        if (e == cudaSuccess)
-            e = cudaMemcpy(g->d_rs_piece, rsp.data(), rsp.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
-    }
-    if (e == cudaSuccess && !ag.empty())
-        e = cudaMemcpy(g->d_ag, ag.data(), ag.size() * sizeof(tide::AgSeg), cudaMemcpyHostToDevice);
-    const auto& agr = g->plan.ag_run;
-    if (e == cudaSuccess && !agr.empty()) {
-        e = cudaMalloc(&g->d_ag_run, agr.size() * sizeof(int32_t));
-        if (e == cudaSuccess)
-            e = cudaMemcpy(g->d_ag_run, agr.data(), agr.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
-    }
-    const auto& rb = g->plan.rs_bulk;
-    if (e == cudaSuccess && !rb.empty()) {
-        e = cudaMalloc(&g->d_rs_bulk, rb.size() * sizeof(tide::RsSeg));
-        if (e == cudaSuccess)
-            e = cudaMemcpy(g->d_rs_bulk, rb.data(), rb.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
-        const auto& rp = g->plan.rs_bulk_piece;
-        if (e == cudaSuccess) e = cudaMalloc(&g->d_rs_bulk_piece, rp.size() * sizeof(int32_t));
-        if (e == cudaSuccess)
-            e = cudaMemcpy(g->d_rs_bulk_piece, rp.data(), rp.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
-    }
-    const auto& sl = g->plan.rs_slots;
-    const auto& slp = g->plan.rs_slot_piece;
-    if (e == cudaSuccess && !sl.empty() && !slp.empty()) {
-        e = cudaMalloc(&g->d_rs_slots, sl.size() * sizeof(tide::RsSeg));
-        if (e == cudaSuccess)
-            e = cudaMemcpy(g->d_rs_slots, sl.data(), sl.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
-        if (e == cudaSuccess) e = cudaMalloc(&g->d_rs_slot_piece, slp.size() * sizeof(int32_t));
-        if (e == cudaSuccess)
-            e = cudaMemcpy(g->d_rs_slot_piece, slp.data(), slp.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
-    }
-    const auto& ab = g->plan.ag_bulk;
-    if (e == cudaSuccess && !ab.empty()) {
-        e = cudaMalloc(&g->d_ag_bulk, ab.size() * sizeof(tide::AgSeg));
-        if (e == cudaSuccess)
-            e = cudaMemcpy(g->d_ag_bulk, ab.data(), ab.size() * sizeof(tide::AgSeg), cudaMemcpyHostToDevice);
-    }
-    if (e == cudaSuccess) e = cudaMalloc(&g->d_status, sizeof(int));
-    if (e == cudaSuccess) e = cudaMemset(g->d_status, 0, sizeof(int));
-    // a table holds the R*P gradient pointers + R shard pointers (reduce-scatter) or R + P
-    // pointers (all-gather)
-    g->slot_cap = size_t(R) * P + R + P;
-    for (Slot& s : g->slots) {
-        if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&s.host), g->slot_cap * sizeof(void*), cudaHostAllocDefault);
-        if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s.dev), g->slot_cap * sizeof(void*));
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming);
-    }
-    if (e != cudaSuccess) {
-        release(g);
-        return e == cudaErrorMemoryAllocation ? (g_last_cuda_error = int(e), TIDE_ENOMEM) : cuda_fail(e);
-    }
-    *out = g;
-    return TIDE_OK;
+        tide_group* g = new (std::nothrow) tide_group();
+        if (!g) return TIDE_ENOMEM;
+        g->plan = std::move(pl);
+        g->flags = flags;
+        if (flags & TIDE_FLAG_OVERLAP) g->ce_lanes = 1;
+        cudaError_t e = cudaGetDevice(&g->device);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g->sm_count, cudaDevAttrMultiProcessorCount, g->device);
+        if (e != cudaSuccess) {
+            release(g);
+            return cuda_fail(e);
+        }
+        const auto& rs = g->plan.rs;
+        const auto& ag = g->plan.ag;
+        e = cudaMalloc(&g->d_rs, std::max<size_t>(1, rs.size()) * sizeof(tide::RsSeg));
+        if (e == cudaSuccess) e = cudaMalloc(&g->d_ag, std::max<size_t>(1, ag.size()) * sizeof(tide::AgSeg));
+        if (e == cudaSuccess && !rs.empty())
+            e = cudaMemcpy(g->d_rs, rs.data(), rs.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
+        const auto& rsp = g->plan.rs_piece;
+        if (e == cudaSuccess && !rsp.empty()) {
+            e = cudaMalloc(&g->d_rs_piece, rsp.size() * sizeof(int32_t));
+            if (e == cudaSuccess)
+                e = cudaMemcpy(g->d_rs_piece, rsp.data(), rsp.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+        }
+        if (e == cudaSuccess && !ag.empty())
+            e = cudaMemcpy(g->d_ag, ag.data(), ag.size() * sizeof(tide::AgSeg), cudaMemcpyHostToDevice);
+        const auto& agr = g->plan.ag_run;
+        if (e == cudaSuccess && !agr.empty()) {
+            e = cudaMalloc(&g->d_ag_run, agr.size() * sizeof(int32_t));
+            if (e == cudaSuccess)
+                e = cudaMemcpy(g->d_ag_run, agr.data(), agr.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+        }
+        const auto& rb = g->plan.rs_bulk;
+        if (e == cudaSuccess && !rb.empty()) {
+            e = cudaMalloc(&g->d_rs_bulk, rb.size() * sizeof(tide::RsSeg));
+            if (e == cudaSuccess)
+                e = cudaMemcpy(g->d_rs_bulk, rb.data(), rb.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
+            const auto& rp = g->plan.rs_bulk_piece;
+            if (e == cudaSuccess) e = cudaMalloc(&g->d_rs_bulk_piece, rp.size() * sizeof(int32_t));
+            if (e == cudaSuccess)
+                e = cudaMemcpy(g->d_rs_bulk_piece, rp.data(), rp.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+        }
+        const auto& sl = g->plan.rs_slots;
+        const auto& slp = g->plan.rs_slot_piece;
+        if (e == cudaSuccess && !sl.empty() && !slp.empty()) {
+            e = cudaMalloc(&g->d_rs_slots, sl.size() * sizeof(tide::RsSeg));
+            if (e == cudaSuccess)
+                e = cudaMemcpy(g->d_rs_slots, sl.data(), sl.size() * sizeof(tide::RsSeg), cudaMemcpyHostToDevice);
+            if (e == cudaSuccess) e = cudaMalloc(&g->d_rs_slot_piece, slp.size() * sizeof(int32_t));
+            if (e == cudaSuccess)
+                e = cudaMemcpy(g->d_rs_slot_piece, slp.data(), slp.size() * sizeof(int32_t), cudaMemcpyHostToDevice);
+        }
+        const auto& ab = g->plan.ag_bulk;
+        if (e == cudaSuccess && !ab.empty()) {
+            e = cudaMalloc(&g->d_ag_bulk, ab.size() * sizeof(tide::AgSeg));
+            if (e == cudaSuccess)
+                e = cudaMemcpy(g->d_ag_bulk, ab.data(), ab.size() * sizeof(tide::AgSeg), cudaMemcpyHostToDevice);
+        }
+        if (e == cudaSuccess) e = cudaMalloc(&g->d_status, sizeof(int));
+        if (e == cudaSuccess) e = cudaMemset(g->d_status, 0, sizeof(int));
+        // a table holds the R*P gradient pointers + R shard pointers (reduce-scatter) or R + P
+        // pointers (all-gather)
+        g->slot_cap = size_t(R) * P + R + P;
+        for (Slot& s : g->slots) {
+            if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&s.host), g->slot_cap * sizeof(void*), cudaHostAllocDefault);
+            if (e == cudaSuccess) e = cudaMalloc(reinterpret_cast<void**>(&s.dev), g->slot_cap * sizeof(void*));
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.done, cudaEventDisableTiming);
+        }
+        if (e != cudaSuccess) {
+            release(g);
+            return e == cudaErrorMemoryAllocation ? (g_last_cuda_error = int(e), TIDE_ENOMEM) : cuda_fail(e);
+        }
+        *out = g;
+        return TIDE_OK;
+    });
 }
 
 int tide_group_destroy(tide_group_t g) {
@@ -470,182 +487,190 @@ int tide_group_get_ctas(tide_group_t g, int32_t* rs_ctas, int32_t* ag_ctas) {
 }
 
 int tide_reduce_scatter(tide_group_t g, const void* const* grads, void* const* shards, void* stream) {
-    if (!g || !grads || !shards) return TIDE_EINVAL;
-    std::lock_guard<std::mutex> lock(g->mu);
-    const int R = g->plan.R, P = g->plan.P;
-    std::vector<const void*> table(size_t(R) * P + R);
-    bool aligned = true;
-    for (size_t i = 0; i < size_t(R) * P; ++i) {
-        if (!grads[i] || !elem_aligned(grads[i], 2)) return TIDE_EINVAL;
-        table[i] = grads[i];
-        aligned &= aligned16(grads[i]);
-    }
-    // the kernels store the sums with whatever vectors each shard address allows, so only the
-    // gradients' alignment decides between the vector paths and the element-wise one
-    for (int d = 0; d < R; ++d) {
-        if (!shards[d] || !elem_aligned(shards[d], 4)) return TIDE_EINVAL;
-        table[size_t(R) * P + d] = shards[d];
-    }
-    if (!aligned && (g->flags & TIDE_FLAG_VEC_STRICT)) return TIDE_EALIGN;
-    int rc = check_device(g);
-    if (rc != TIDE_OK) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int k = 0;
-    if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
-    void** dev = g->slots[k].dev;
-    const auto* gp = reinterpret_cast<const uint16_t* const*>(dev);
-    auto* sp = reinterpret_cast<float* const*>(dev + size_t(R) * P);
-    cudaError_t e;
-    if (use_bulk(g, aligned)) {
-        const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, true);
-        auto* launch = rs_bulk_launcher(g);
-        e = launch(g->d_rs_bulk, g->d_rs_bulk_piece, g->plan.rs_bulk_chunks, gp, sp, R, P, 1, ctas, g->d_status,
-                   g->timeout_ns, (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
-    } else {
-        const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, false);
-        e = tide::launch_reduce_scatter(g->d_rs, int(g->plan.rs.size()), g->d_rs_piece, g->plan.rs_chunks, gp, sp,
-                                        R, P, aligned ? 1 : 0, ctas, st);
-    }
-    if (e != cudaSuccess) return cuda_fail(e);
-    return finish_slot(g, k, st);
+    return no_throw([&]() -> int {
+        if (!g || !grads || !shards) return TIDE_EINVAL;
+        std::lock_guard<std::mutex> lock(g->mu);
+        const int R = g->plan.R, P = g->plan.P;
+        std::vector<const void*> table(size_t(R) * P + R);
+        bool aligned = true;
+        for (size_t i = 0; i < size_t(R) * P; ++i) {
+            if (!grads[i] || !elem_aligned(grads[i], 2)) return TIDE_EINVAL;
+            table[i] = grads[i];
+            aligned &= aligned16(grads[i]);
+        }
+        // the kernels store the sums with whatever vectors each shard address allows, so only the
+        // gradients' alignment decides between the vector paths and the element-wise one
+        for (int d = 0; d < R; ++d) {
+            if (!shards[d] || !elem_aligned(shards[d], 4)) return TIDE_EINVAL;
+            table[size_t(R) * P + d] = shards[d];
+        }
+        if (!aligned && (g->flags & TIDE_FLAG_VEC_STRICT)) return TIDE_EALIGN;
+        int rc = check_device(g);
+        if (rc != TIDE_OK) return rc;
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        int k = 0;
+        if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
+        void** dev = g->slots[k].dev;
+        const auto* gp = reinterpret_cast<const uint16_t* const*>(dev);
+        auto* sp = reinterpret_cast<float* const*>(dev + size_t(R) * P);
+        cudaError_t e;
+        if (use_bulk(g, aligned)) {
+            const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, true);
+            auto* launch = rs_bulk_launcher(g);
+            e = launch(g->d_rs_bulk, g->d_rs_bulk_piece, g->plan.rs_bulk_chunks, gp, sp, R, P, 1, ctas, g->d_status,
+                       g->timeout_ns, (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
+        } else {
+            const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, false);
+            e = tide::launch_reduce_scatter(g->d_rs, int(g->plan.rs.size()), g->d_rs_piece, g->plan.rs_chunks, gp, sp,
+                                            R, P, aligned ? 1 : 0, ctas, st);
+        }
+        if (e != cudaSuccess) return cuda_fail(e);
+        return finish_slot(g, k, st);
+    });
 }
 
 int tide_reduce_scatter_slots(tide_group_t g, int32_t d, const void* const* slots, void* shard, void* stream) {
-    if (!g || !slots || !shard) return TIDE_EINVAL;
-    std::lock_guard<std::mutex> lock(g->mu);
-    const int R = g->plan.R, P = g->plan.P;
-    if (d < 0 || d >= R || !elem_aligned(shard, 4)) return TIDE_EINVAL;
-    std::vector<const void*> table(size_t(R) + 1);
-    bool aligned = true;
-    for (int r = 0; r < R; ++r) {
-        if (!slots[r] || !elem_aligned(slots[r], 2)) return TIDE_EINVAL;
-        table[size_t(r)] = slots[r];
-        aligned &= aligned16(slots[r]);
-    }
-    table[size_t(R)] = shard;
-    if (!aligned && (g->flags & TIDE_FLAG_VEC_STRICT)) return TIDE_EALIGN;
-    if (!g->d_rs_slots || !g->d_rs_slot_piece) return TIDE_EINVAL;
-    int rc = check_device(g);
-    if (rc != TIDE_OK) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int k = 0;
-    if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
-    void** dev = g->slots[k].dev;
-    // one table entry per slot and one shard: the pieces carry p = 0 and d = 0
-    const auto* gp = reinterpret_cast<const uint16_t* const*>(dev);
-    auto* sp = reinterpret_cast<float* const*>(dev + R);
-    const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, true);
-    auto* launch = rs_bulk_launcher(g);
-    cudaError_t e = launch(g->d_rs_slots + size_t(d) * size_t(P), g->d_rs_slot_piece, g->plan.rs_slot_chunks, gp, sp,
-                           R, 1, aligned ? 1 : 0, ctas, g->d_status, g->timeout_ns,
-                           (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return finish_slot(g, k, st);
+    return no_throw([&]() -> int {
+        if (!g || !slots || !shard) return TIDE_EINVAL;
+        std::lock_guard<std::mutex> lock(g->mu);
+        const int R = g->plan.R, P = g->plan.P;
+        if (d < 0 || d >= R || !elem_aligned(shard, 4)) return TIDE_EINVAL;
+        std::vector<const void*> table(size_t(R) + 1);
+        bool aligned = true;
+        for (int r = 0; r < R; ++r) {
+            if (!slots[r] || !elem_aligned(slots[r], 2)) return TIDE_EINVAL;
+            table[size_t(r)] = slots[r];
+            aligned &= aligned16(slots[r]);
+        }
+        table[size_t(R)] = shard;
+        if (!aligned && (g->flags & TIDE_FLAG_VEC_STRICT)) return TIDE_EALIGN;
+        if (!g->d_rs_slots || !g->d_rs_slot_piece) return TIDE_EINVAL;
+        int rc = check_device(g);
+        if (rc != TIDE_OK) return rc;
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        int k = 0;
+        if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
+        void** dev = g->slots[k].dev;
+        // one table entry per slot and one shard: the pieces carry p = 0 and d = 0
+        const auto* gp = reinterpret_cast<const uint16_t* const*>(dev);
+        auto* sp = reinterpret_cast<float* const*>(dev + R);
+        const int ctas = g->rs_ctas ? g->rs_ctas : rs_default_ctas(g, true);
+        auto* launch = rs_bulk_launcher(g);
+        cudaError_t e = launch(g->d_rs_slots + size_t(d) * size_t(P), g->d_rs_slot_piece, g->plan.rs_slot_chunks, gp, sp,
+                               R, 1, aligned ? 1 : 0, ctas, g->d_status, g->timeout_ns,
+                               (g->debug & TIDE_DEBUG_STALL_PRODUCER) ? 1 : 0, st);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return finish_slot(g, k, st);
+    });
 }
 
 int tide_all_gather(tide_group_t g, const void* const* shards, void* const* params, void* stream) {
-    if (!g || !shards || !params) return TIDE_EINVAL;
-    std::lock_guard<std::mutex> lock(g->mu);
-    const int R = g->plan.R, P = g->plan.P;
-    std::vector<const void*> table(size_t(R) + P);
-    bool aligned = true;
-    for (int r = 0; r < R; ++r) {
-        if (!shards[r] || !elem_aligned(shards[r], 2)) return TIDE_EINVAL;
-        table[r] = shards[r];
-        aligned &= aligned16(shards[r]);
-    }
-    for (int p = 0; p < P; ++p) {
-        if (!params[p] || !elem_aligned(params[p], 2)) return TIDE_EINVAL;
-        table[size_t(R) + p] = params[p];
-        aligned &= aligned16(params[p]);
-    }
-    if (!aligned && (g->flags & TIDE_FLAG_VEC_STRICT)) return TIDE_EALIGN;
-    int rc = check_device(g);
-    if (rc != TIDE_OK) return rc;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int k = 0;
-    if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
-    void** dev = g->slots[k].dev;
-    const auto* sp = reinterpret_cast<const uint16_t* const*>(dev);
-    auto* pp = reinterpret_cast<uint16_t* const*>(dev + R);
-    cudaError_t e;
-    if (ag_uses_bulk(g, aligned)) {
-        const int ctas = g->ag_ctas ? g->ag_ctas : ag_default_ctas(g, true);
-        e = tide::launch_all_gather_bulk(g->d_ag_bulk, int(g->plan.ag_bulk.size()), g->plan.ag_bulk_chunks, sp, pp,
-                                         ctas, g->d_status, g->timeout_ns, st);
-    } else {
-        const int ctas = g->ag_ctas ? g->ag_ctas : ag_default_ctas(g, false);
-        e = tide::launch_all_gather(g->d_ag, int(g->plan.ag.size()), g->d_ag_run, g->plan.ag_chunks, sp, pp,
-                                    aligned ? 1 : 0, ctas, st);
-    }
-    if (e != cudaSuccess) return cuda_fail(e);
-    return finish_slot(g, k, st);
+    return no_throw([&]() -> int {
+        if (!g || !shards || !params) return TIDE_EINVAL;
+        std::lock_guard<std::mutex> lock(g->mu);
+        const int R = g->plan.R, P = g->plan.P;
+        std::vector<const void*> table(size_t(R) + P);
+        bool aligned = true;
+        for (int r = 0; r < R; ++r) {
+            if (!shards[r] || !elem_aligned(shards[r], 2)) return TIDE_EINVAL;
+            table[r] = shards[r];
+            aligned &= aligned16(shards[r]);
+        }
+        for (int p = 0; p < P; ++p) {
+            if (!params[p] || !elem_aligned(params[p], 2)) return TIDE_EINVAL;
+            table[size_t(R) + p] = params[p];
+            aligned &= aligned16(params[p]);
+        }
+        if (!aligned && (g->flags & TIDE_FLAG_VEC_STRICT)) return TIDE_EALIGN;
+        int rc = check_device(g);
+        if (rc != TIDE_OK) return rc;
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        int k = 0;
+        if ((rc = upload_table(g, table, st, &k)) != TIDE_OK) return rc;
+        void** dev = g->slots[k].dev;
+        const auto* sp = reinterpret_cast<const uint16_t* const*>(dev);
+        auto* pp = reinterpret_cast<uint16_t* const*>(dev + R);
+        cudaError_t e;
+        if (ag_uses_bulk(g, aligned)) {
+            const int ctas = g->ag_ctas ? g->ag_ctas : ag_default_ctas(g, true);
+            e = tide::launch_all_gather_bulk(g->d_ag_bulk, int(g->plan.ag_bulk.size()), g->plan.ag_bulk_chunks, sp, pp,
+                                             ctas, g->d_status, g->timeout_ns, st);
+        } else {
+            const int ctas = g->ag_ctas ? g->ag_ctas : ag_default_ctas(g, false);
+            e = tide::launch_all_gather(g->d_ag, int(g->plan.ag.size()), g->d_ag_run, g->plan.ag_chunks, sp, pp,
+                                        aligned ? 1 : 0, ctas, st);
+        }
+        if (e != cudaSuccess) return cuda_fail(e);
+        return finish_slot(g, k, st);
+    });
 }
 
 int tide_all_gather_ce(tide_group_t g, const void* const* shards, void* const* params, void* stream) {
-    if (!g || !shards || !params) return TIDE_EINVAL;
-    std::lock_guard<std::mutex> lock(g->mu);
-    const tide::Plan& pl = g->plan;
-    const int R = pl.R, P = pl.P;
-    for (int r = 0; r < R; ++r)
-        if (!shards[r]) return TIDE_EINVAL;
-    for (int p = 0; p < P; ++p)
-        if (!params[p]) return TIDE_EINVAL;
-    // Uniform pitch: shards[r] = shards[0] + r * pitch with pitch >= S*2 bytes.
-    const char* base = static_cast<const char*>(shards[0]);
-    const int64_t pitch = R > 1 ? static_cast<const char*>(shards[1]) - base : pl.S * 2;
-    bool uniform = pitch >= pl.S * 2;
-    for (int r = 1; r < R && uniform; ++r) uniform = static_cast<const char*>(shards[r]) == base + int64_t(r) * pitch;
-    if (g->flags & TIDE_FLAG_CE_2D) {
-        if (!uniform && (g->flags & TIDE_FLAG_CE_STRICT)) return TIDE_ELAYOUT;
-    } else if ((g->flags & TIDE_FLAG_CE_1D) || !ce_auto_prefers_2d(g)) {
-        uniform = false;  // one 1-D copy per (rank, parameter) run
-    }
-    int rc = check_device(g);
-    if (rc != TIDE_OK) return rc;
-    CeLanes lanes{g, static_cast<cudaStream_t>(stream)};
-    if ((rc = lanes.begin()) != TIDE_OK) return rc;
-    int64_t copies = 0;
-    for (int p = 0; p < P; ++p) {
-        char* dst = static_cast<char*>(params[p]);
-        const int64_t piece_bytes = pl.s[p] * 2;
-        if (uniform) {
-            // ranks 0 .. f-1 hold full pieces of m_p rows: one 2-D copy per band of ranks (one band
-            // by default: the whole parameter in one strided copy), source rows `pitch` apart,
-            // destination rows contiguous
-            const int64_t f = pl.rows[p] / pl.m[p];
-            const int64_t nb = std::min<int64_t>(g->ce_bands, f);
-            for (int64_t b = 0; b < nb; ++b) {
-                const int64_t r0 = f * b / nb, r1 = f * (b + 1) / nb;
-                TIDE_LANE_COPY(lanes, cudaMemcpy2DAsync(dst + r0 * piece_bytes, size_t(piece_bytes),
-                                                        base + r0 * pitch + pl.o[p] * 2, size_t(pitch),
-                                                        size_t(piece_bytes), size_t(r1 - r0), cudaMemcpyDeviceToDevice,
-                                                        lanes.pick((r1 - r0) * piece_bytes)));
-                ++copies;
-            }
-            const int64_t rest = pl.rows[p] - f * pl.m[p];
-            if (rest > 0) {
-                const int64_t bytes = rest * pl.row_len[p] * 2;
-                TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst + f * piece_bytes, base + f * pitch + pl.o[p] * 2,
-                                                      size_t(bytes), cudaMemcpyDeviceToDevice, lanes.pick(bytes)));
-                ++copies;
-            }
-        } else {
-            for (int r = 0; r < R; ++r) {
-                const int64_t v = tide::valid_rows(pl.rows[p], pl.m[p], r);
-                if (v == 0) continue;
-                const int64_t bytes = v * pl.row_len[p] * 2;
-                TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst + r * piece_bytes,
-                                                      static_cast<const char*>(shards[r]) + pl.o[p] * 2, size_t(bytes),
-                                                      cudaMemcpyDeviceToDevice, lanes.pick(bytes)));
-                ++copies;
+    return no_throw([&]() -> int {
+        if (!g || !shards || !params) return TIDE_EINVAL;
+        std::lock_guard<std::mutex> lock(g->mu);
+        const tide::Plan& pl = g->plan;
+        const int R = pl.R, P = pl.P;
+        for (int r = 0; r < R; ++r)
+            if (!shards[r]) return TIDE_EINVAL;
+        for (int p = 0; p < P; ++p)
+            if (!params[p]) return TIDE_EINVAL;
+        // Uniform pitch: shards[r] = shards[0] + r * pitch with pitch >= S*2 bytes.
+        const char* base = static_cast<const char*>(shards[0]);
+        const int64_t pitch = R > 1 ? static_cast<const char*>(shards[1]) - base : pl.S * 2;
+        bool uniform = pitch >= pl.S * 2;
+        for (int r = 1; r < R && uniform; ++r) uniform = static_cast<const char*>(shards[r]) == base + int64_t(r) * pitch;
+        if (g->flags & TIDE_FLAG_CE_2D) {
+            if (!uniform && (g->flags & TIDE_FLAG_CE_STRICT)) return TIDE_ELAYOUT;
+        } else if ((g->flags & TIDE_FLAG_CE_1D) || !ce_auto_prefers_2d(g)) {
+            uniform = false;  // one 1-D copy per (rank, parameter) run
+        }
+        int rc = check_device(g);
+        if (rc != TIDE_OK) return rc;
+        CeLanes lanes{g, static_cast<cudaStream_t>(stream)};
+        if ((rc = lanes.begin()) != TIDE_OK) return rc;
+        int64_t copies = 0;
+        for (int p = 0; p < P; ++p) {
+            char* dst = static_cast<char*>(params[p]);
+            const int64_t piece_bytes = pl.s[p] * 2;
+            if (uniform) {
+                // ranks 0 .. f-1 hold full pieces of m_p rows: one 2-D copy per band of ranks (one band
+                // by default: the whole parameter in one strided copy), source rows `pitch` apart,
+                // destination rows contiguous
+                const int64_t f = pl.rows[p] / pl.m[p];
+                const int64_t nb = std::min<int64_t>(g->ce_bands, f);
+                for (int64_t b = 0; b < nb; ++b) {
+                    const int64_t r0 = f * b / nb, r1 = f * (b + 1) / nb;
+                    TIDE_LANE_COPY(lanes, cudaMemcpy2DAsync(dst + r0 * piece_bytes, size_t(piece_bytes),
+                                                            base + r0 * pitch + pl.o[p] * 2, size_t(pitch),
+                                                            size_t(piece_bytes), size_t(r1 - r0), cudaMemcpyDeviceToDevice,
+                                                            lanes.pick((r1 - r0) * piece_bytes)));
+                    ++copies;
+                }
+                const int64_t rest = pl.rows[p] - f * pl.m[p];
+                if (rest > 0) {
+                    const int64_t bytes = rest * pl.row_len[p] * 2;
+                    TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst + f * piece_bytes, base + f * pitch + pl.o[p] * 2,
+                                                          size_t(bytes), cudaMemcpyDeviceToDevice, lanes.pick(bytes)));
+                    ++copies;
+                }
+            } else {
+                for (int r = 0; r < R; ++r) {
+                    const int64_t v = tide::valid_rows(pl.rows[p], pl.m[p], r);
+                    if (v == 0) continue;
+                    const int64_t bytes = v * pl.row_len[p] * 2;
+                    TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst + r * piece_bytes,
+                                                          static_cast<const char*>(shards[r]) + pl.o[p] * 2, size_t(bytes),
+                                                          cudaMemcpyDeviceToDevice, lanes.pick(bytes)));
+                    ++copies;
+                }
             }
         }
-    }
-    if ((rc = lanes.end()) != TIDE_OK) return rc;
-    g->last_ce_copies = copies;
-    g->last_ce_uniform = uniform ? 1 : 0;
-    return TIDE_OK;
+        if ((rc = lanes.end()) != TIDE_OK) return rc;
+        g->last_ce_copies = copies;
+        g->last_ce_uniform = uniform ? 1 : 0;
+        return TIDE_OK;
+    });
 }
 
 int tide_group_set_rs_variant(tide_group_t g, int32_t variant) {
@@ -719,61 +744,65 @@ int tide_group_device_status(tide_group_t g, int32_t* status) {
 
 int tide_stage_into_slots(tide_group_t g, const void* const* grads, void* const* slots, int64_t slot_elems,
                           void** staged, void* stream) {
-    if (!g || !grads || !slots || !staged) return TIDE_EINVAL;
-    std::lock_guard<std::mutex> lock(g->mu);
-    const tide::Plan& pl = g->plan;
-    const int R = pl.R, P = pl.P;
-    if (slot_elems < pl.U) return TIDE_ERANGE;
-    for (size_t i = 0; i < size_t(R) * P; ++i)
-        if (!grads[i]) return TIDE_EINVAL;
-    for (int r = 0; r < R; ++r)
-        if (!slots[r]) return TIDE_EINVAL;
-    int rc = check_device(g);
-    if (rc != TIDE_OK) return rc;
-    CeLanes lanes{g, static_cast<cudaStream_t>(stream)};
-    if ((rc = lanes.begin()) != TIDE_OK) return rc;
-    // parameter p of rank r lands at slot_r + (rows_0*L_0 + ... + rows_{p-1}*L_{p-1}) elements:
-    // the unsharded group, packed without padding, 16-byte aligned when every size is a multiple of 8
-    int64_t off = 0;
-    for (int p = 0; p < P; ++p) {
-        const int64_t n = pl.rows[p] * pl.row_len[p];
-        for (int r = 0; r < R; ++r) {
-            char* dst = static_cast<char*>(slots[r]) + off * 2;
-            TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst, grads[size_t(r) * P + p], size_t(n) * 2,
-                                                  cudaMemcpyDeviceToDevice, lanes.pick(n * 2)));
-            staged[size_t(r) * P + p] = dst;
+    return no_throw([&]() -> int {
+        if (!g || !grads || !slots || !staged) return TIDE_EINVAL;
+        std::lock_guard<std::mutex> lock(g->mu);
+        const tide::Plan& pl = g->plan;
+        const int R = pl.R, P = pl.P;
+        if (slot_elems < pl.U) return TIDE_ERANGE;
+        for (size_t i = 0; i < size_t(R) * P; ++i)
+            if (!grads[i]) return TIDE_EINVAL;
+        for (int r = 0; r < R; ++r)
+            if (!slots[r]) return TIDE_EINVAL;
+        int rc = check_device(g);
+        if (rc != TIDE_OK) return rc;
+        CeLanes lanes{g, static_cast<cudaStream_t>(stream)};
+        if ((rc = lanes.begin()) != TIDE_OK) return rc;
+        // parameter p of rank r lands at slot_r + (rows_0*L_0 + ... + rows_{p-1}*L_{p-1}) elements:
+        // the unsharded group, packed without padding, 16-byte aligned when every size is a multiple of 8
+        int64_t off = 0;
+        for (int p = 0; p < P; ++p) {
+            const int64_t n = pl.rows[p] * pl.row_len[p];
+            for (int r = 0; r < R; ++r) {
+                char* dst = static_cast<char*>(slots[r]) + off * 2;
+                TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst, grads[size_t(r) * P + p], size_t(n) * 2,
+                                                      cudaMemcpyDeviceToDevice, lanes.pick(n * 2)));
+                staged[size_t(r) * P + p] = dst;
+            }
+            off += n;
         }
-        off += n;
-    }
-    return lanes.end();
+        return lanes.end();
+    });
 }
 
 int tide_stage_slices(tide_group_t g, int32_t d, const void* const* grads, void* const* slots, void* stream) {
-    if (!g || !grads || !slots) return TIDE_EINVAL;
-    std::lock_guard<std::mutex> lock(g->mu);
-    const tide::Plan& pl = g->plan;
-    const int R = pl.R, P = pl.P;
-    if (d < 0 || d >= R) return TIDE_EINVAL;
-    for (size_t i = 0; i < size_t(R) * P; ++i)
-        if (!grads[i] || !elem_aligned(grads[i], 2)) return TIDE_EINVAL;
-    for (int r = 0; r < R; ++r)
-        if (!slots[r] || !elem_aligned(slots[r], 2)) return TIDE_EINVAL;
-    int rc = check_device(g);
-    if (rc != TIDE_OK) return rc;
-    CeLanes lanes{g, static_cast<cudaStream_t>(stream)};
-    if ((rc = lanes.begin()) != TIDE_OK) return rc;
-    // contributors d+1, ..., R-1, 0, ..., d; within one, parameters in order
-    for (int k = 1; k <= R; ++k) {
-        const int r = (d + k) % R;
-        for (int p = 0; p < P; ++p) {
-            const int64_t n = tide::valid_rows(pl.rows[p], pl.m[p], d) * pl.row_len[p];
-            if (n == 0) continue;
-            const char* src = static_cast<const char*>(grads[size_t(r) * P + p]) + int64_t(d) * pl.s[p] * 2;
-            char* dst = static_cast<char*>(slots[r]) + pl.o[p] * 2;
-            TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst, src, size_t(n) * 2, cudaMemcpyDeviceToDevice, lanes.pick(n * 2)));
+    return no_throw([&]() -> int {
+        if (!g || !grads || !slots) return TIDE_EINVAL;
+        std::lock_guard<std::mutex> lock(g->mu);
+        const tide::Plan& pl = g->plan;
+        const int R = pl.R, P = pl.P;
+        if (d < 0 || d >= R) return TIDE_EINVAL;
+        for (size_t i = 0; i < size_t(R) * P; ++i)
+            if (!grads[i] || !elem_aligned(grads[i], 2)) return TIDE_EINVAL;
+        for (int r = 0; r < R; ++r)
+            if (!slots[r] || !elem_aligned(slots[r], 2)) return TIDE_EINVAL;
+        int rc = check_device(g);
+        if (rc != TIDE_OK) return rc;
+        CeLanes lanes{g, static_cast<cudaStream_t>(stream)};
+        if ((rc = lanes.begin()) != TIDE_OK) return rc;
+        // contributors d+1, ..., R-1, 0, ..., d; within one, parameters in order
+        for (int k = 1; k <= R; ++k) {
+            const int r = (d + k) % R;
+            for (int p = 0; p < P; ++p) {
+                const int64_t n = tide::valid_rows(pl.rows[p], pl.m[p], d) * pl.row_len[p];
+                if (n == 0) continue;
+                const char* src = static_cast<const char*>(grads[size_t(r) * P + p]) + int64_t(d) * pl.s[p] * 2;
+                char* dst = static_cast<char*>(slots[r]) + pl.o[p] * 2;
+                TIDE_LANE_COPY(lanes, cudaMemcpyAsync(dst, src, size_t(n) * 2, cudaMemcpyDeviceToDevice, lanes.pick(n * 2)));
+            }
         }
-    }
-    return lanes.end();
+        return lanes.end();
+    });
 }
 
 int tide_group_last_ce_copies(tide_group_t g, int64_t* copies, int32_t* uniform_pitch) {
