@@ -70,7 +70,7 @@ extern "C" {
 /*
  * Interference-first defaults, for collectives that run beside compute (Fig. 3, Fig. 4, Table 4):
  * both SM kernels launch about a ninth of the SMs as CTAs (16 on a 152-SM GB300) instead of filling
- * the GPU, and tide_all_gather_ce uses one copy-engine lane and the 1-D form.  Measured on GB300
+ * the GPU, and tide_all_gather_ce uses one copy-engine lane (its form rule unchanged).  Measured on GB300
  * beside a single-wave cuBLAS bf16 GEMM (4096 x 4096 x 8192): the GEMM slows by a few percent
  * instead of +1400 % (reduce-scatter), +290 % (SM placement) and +60 % (copy engines, 8 lanes) at
  * the throughput-first defaults, while the collectives move a quarter to two thirds as many bytes
@@ -215,8 +215,9 @@ int tide_all_gather(tide_group_t g, const void *const *shards, void *const *para
  * TIDE_FLAG_CE_1D or TIDE_FLAG_CE_2D fixes the form (TIDE_FLAG_CE_2D falls back to 1-D without a
  * uniform pitch, or returns TIDE_ELAYOUT under TIDE_FLAG_CE_STRICT).  With neither flag the group
  * takes the 2-D form when the pitch is uniform and its valid runs average less than 4 MiB, else the
- * 1-D form; under TIDE_FLAG_OVERLAP always the 1-D form (strided copies slow a concurrent GEMM far
- * more per byte moved: +142-149 % against +4-7 % over one lane on the Llama-3.1-70B layer).
+ * 1-D form; the same under TIDE_FLAG_OVERLAP, over one lane (there, beside a single-wave GEMM, strided
+ * copies of long runs cost far more than 1-D copies: +138 % against +5 % on the Llama-3.1-70B layer;
+ * those of short runs no more: +1.3 % on the Qwen3 MoE layer, moving 4x as much).
  */
 int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *params,
                        void *stream);

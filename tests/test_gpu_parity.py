@@ -310,7 +310,7 @@ def _ce_auto_expects_2d(g, lay):
                          ids=["llama70b-full", "qwen3moe-div4", "tiny"])
 def test_all_gather_ce_default_form(tide, g):
     """No form flag and a uniform pitch: the 2-D form for groups of short runs, the 1-D form for long
-    runs (the full Llama-3.1-70B layer); under TIDE_FLAG_OVERLAP always the 1-D form over one lane."""
+    runs (the full Llama-3.1-70B layer); the same rule under TIDE_FLAG_OVERLAP."""
     lay = oracle.plan(g.R, g.rows, g.row_len)
     if lay.U > (1 << 26):  # full-size group: the form choice only, through one unchecked call
         G = tide.Group(g.R, list(zip(g.rows, g.row_len)))
@@ -326,7 +326,23 @@ def test_all_gather_ce_default_form(tide, g):
     copies, uniform = run_ag(tide, g, ce=True)
     assert uniform == _ce_auto_expects_2d(g, lay)
     copies, uniform = run_ag(tide, g, ce=True, flags=tide.TIDE_FLAG_OVERLAP)
-    assert not uniform
+    assert uniform == _ce_auto_expects_2d(g, lay)
+
+
+@pytest.mark.parametrize("g", [group("llama70b").scaled(32), group("qwen3moe").scaled(16), group("tiny")],
+                         ids=lambda g: g.name)
+def test_overlap_mode_defaults_and_parity(tide, g):
+    """TIDE_FLAG_OVERLAP: both SM kernels default to a ninth of the SMs, the copy engines to one lane;
+    all three collectives still give the oracle's bits with the defaults."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    G = tide.Group(g.R, list(zip(g.rows, g.row_len)), tide.TIDE_FLAG_OVERLAP)
+    assert G.get_ctas() == (max(1, sms // 9), max(1, sms // 9))
+    G.close()
+    run_rs(tide, g, flags=tide.TIDE_FLAG_OVERLAP)
+    run_ag(tide, g, flags=tide.TIDE_FLAG_OVERLAP)
+    copies, uniform = run_ag(tide, g, ce=True, flags=tide.TIDE_FLAG_OVERLAP)
+    lay = oracle.plan(g.R, g.rows, g.row_len)
+    assert uniform == _ce_auto_expects_2d(g, lay)
 
 
 @pytest.mark.parametrize("bands", [2, 3, 64])
