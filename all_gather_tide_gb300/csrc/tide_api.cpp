@@ -270,9 +270,9 @@ bool ag_uses_bulk(const tide_group* g, bool aligned) {
 // 3.7 TB/s; 8B layer, 6 MB: 5.0 against 3.6; Wan R = 8, 5.6 MB: 3.7 against 3.5), the 2-D form below
 // (Wan R = 16, 2.8 MB runs: 3.5 against 2.5; Qwen3 MoE layer, 0.4 MB: 2.6 against 0.37).  The same
 // rule holds over the one lane of TIDE_FLAG_OVERLAP beside a single-wave GEMM: strided copies of
-// long runs slow it far more than 1-D copies (70B layer +138 % against +5 %, 8B +26 % against +4 %,
-// Wan R = 8 +9 % against +3 %), those of short runs no more (Wan R = 16 / 32 / 64 +3.5 / +2.5 / +1.2 %,
-// Qwen3 +1.3 %) while they move up to 4x as much beside it (Qwen3: 0.75 against 0.19 TB/s).
+// long runs slow it far more than 1-D copies (70B layer +144 % against +6 %, 8B +24 % against +5 %,
+// Wan R = 8 +13 % against +6 %), those of short runs no more (Wan R = 16 / 32 / 64 +2.6 / +1.4 / +2.1 %,
+// Qwen3 +1.8 %) while they move up to 4x as much beside it (Qwen3: 0.75 against 0.19 TB/s).
 constexpr int64_t kCeLongRunBytes = int64_t(4) << 20;
 
 bool ce_auto_prefers_2d(const tide_group* g) {

@@ -741,6 +741,19 @@ def interference(G, buf, stream, dev, args):
     ov["flag"] = "TIDE_FLAG_OVERLAP"
     out["overlap_mode"] = ov
     Gov.close()
+    if args.overlap_ce_forms:
+        # the copy-engine placement over overlap mode's one lane in each form, whatever the rule picks
+        forms = {}
+        for form, extra in (("1d", tide.TIDE_FLAG_CE_1D), ("2d", tide.TIDE_FLAG_CE_2D)):
+            Gf = tide.Group(G.R, list(zip(G.rows, G.row_len)), tide.TIDE_FLAG_OVERLAP | extra)
+            launch = lambda: [Gf.all_gather_ce(buf.ag_list, buf.params, stream) for _ in range(8)]
+            ms = alone_ms(launch)
+            conc = concurrent(launch, "ce")
+            forms[form] = dict(gbs_alone=8 * b_ag / (ms * 1e-3) / 1e9,
+                               gbs_beside_gemm=8 * b_ag / (conc["collective_ms"] * 1e-3) / 1e9, **conc)
+            forms[form]["copies"], forms[form]["uniform_pitch"] = Gf.last_ce_copies()
+            Gf.close()
+        out["overlap_ce_forms"] = forms
     return out
 
 
@@ -1373,6 +1386,8 @@ def main():
     ap.add_argument("--sweep-ag", type=int, nargs="*", default=[8, 16, 24, 32, 64, 152, 608])
     ap.add_argument("--probes", action="store_true", help="spin-CTA curve, SM-id probe and Table 4 victims")
     ap.add_argument("--slot-reuse", action="store_true", help="Slot-Reuse staging leg")
+    ap.add_argument("--overlap-ce-forms", action="store_true",
+                    help="copy-engine placement over one lane in both forms beside the GEMM")
     ap.add_argument("--spin-ctas", type=int, nargs="*", default=[1, 4, 8, 12, 16, 20, 24, 32, 48, 64, 96, 152])
     ap.add_argument("--no-interference", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -216,8 +216,8 @@ int tide_all_gather(tide_group_t g, const void *const *shards, void *const *para
  * uniform pitch, or returns TIDE_ELAYOUT under TIDE_FLAG_CE_STRICT).  With neither flag the group
  * takes the 2-D form when the pitch is uniform and its valid runs average less than 4 MiB, else the
  * 1-D form; the same under TIDE_FLAG_OVERLAP, over one lane (there, beside a single-wave GEMM, strided
- * copies of long runs cost far more than 1-D copies: +138 % against +5 % on the Llama-3.1-70B layer;
- * those of short runs no more: +1.3 % on the Qwen3 MoE layer, moving 4x as much).
+ * copies of long runs cost far more than 1-D copies: +144 % against +6 % on the Llama-3.1-70B layer;
+ * those of short runs no more: +1.8 % on the Qwen3 MoE layer, moving 4x as much).
  */
 int tide_all_gather_ce(tide_group_t g, const void *const *shards, void *const *params,
                        void *stream);
