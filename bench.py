@@ -738,6 +738,30 @@ def interference(G, buf, stream, dev, args):
                         gbs_beside_gemm=nbytes / (conc["collective_ms"] * 1e-3) / 1e9, **conc)
     ov["all_gather_sm"]["kernel"] = "all_gather_bulk_kernel" if Gov.ag_kernel() == tide.TIDE_AG_BULK else "all_gather_kernel"
     ov["all_gather_ce"]["copies"], ov["all_gather_ce"]["uniform_pitch"] = Gov.last_ce_copies()
+    # one layer's reduce-scatter and another's all-gather at once, as FSDP overlaps them: the
+    # reduce-scatter on its 16 CTAs and copy-engine placements on a second stream until it ends
+    s_b = torch.cuda.Stream(device=dev)
+    ce_ms = alone_ms(lambda: Gov.all_gather_ce(buf.ag_list, buf.params, stream))
+    n_ce = max(1, int(round(ov["reduce_scatter"]["collective_ms"] / max(ce_ms, 1e-3))))
+
+    def both():
+        start = torch.cuda.Event()
+        start.record(stream)
+        s_b.wait_event(start)
+        Gov.reduce_scatter(buf.grads, buf.shard_list, stream)
+        with torch.cuda.stream(s_b):
+            for _ in range(n_ce):
+                Gov.all_gather_ce(buf.ag_list, buf.params, s_b)
+        end = torch.cuda.Event()
+        end.record(s_b)
+        stream.wait_event(end)
+
+    ms = alone_ms(both)
+    conc = concurrent(both, "rs+ce")
+    nbytes = b_rs + n_ce * b_ag
+    ov["reduce_scatter_with_ce_placement"] = dict(
+        placements=n_ce, gbs_alone=nbytes / (ms * 1e-3) / 1e9,
+        gbs_beside_gemm=nbytes / (conc["collective_ms"] * 1e-3) / 1e9, **conc)
     ov["flag"] = "TIDE_FLAG_OVERLAP"
     out["overlap_mode"] = ov
     Gov.close()
